@@ -230,12 +230,11 @@ int oracle_decode(const uint8_t* pool, int dtype, int num_layers,
         denom += s[i];
       }
       double* o = out + (static_cast<int64_t>(r) * num_heads + h) * kDimCkv;
-      for (int d = 0; d < kDimCkv; ++d) {
-        double acc = 0.0;
-        for (int i = 0; i < n; ++i)
-          acc += s[i] * K[static_cast<size_t>(i) * kDimRow + d];
-        o[d] = acc / denom;
-      }
+      std::vector<double> acc(kDimCkv, 0.0);
+      for (int i = 0; i < n; ++i)
+        for (int d = 0; d < kDimCkv; ++d)
+          acc[d] += s[i] * K[static_cast<size_t>(i) * kDimRow + d];
+      for (int d = 0; d < kDimCkv; ++d) o[d] = acc[d] / denom;
       if (lse) lse[static_cast<int64_t>(r) * num_heads + h] = m + std::log(denom);
     }
   }

@@ -1,0 +1,196 @@
+// Host side of the C ABI declared in include/mla_decode.h: argument checks,
+// workspace layout, TMA tensor maps, kernel launches. No allocation, no
+// stream synchronisation (except mla_get_error).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include "../../include/mla_decode.h"
+#include "mla_internal.h"
+
+namespace {
+
+using mla::WsHeader;
+using mla::WsLayout;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D row-major map: rows x cols elements, row pitch `pitch_bytes`, box
+// {box_cols, box_rows}, 128-byte swizzle, zero fill out of bounds.
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t rows, uint64_t cols,
+                 uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_pool(const mla_kv_pool* pool) {
+  if (!pool || !pool->data || pool->num_layers <= 0 || pool->num_pages <= 0) return false;
+  if (pool->page_size != 16 && pool->page_size != 32 && pool->page_size != 64 && pool->page_size != 128)
+    return false;
+  if (pool->dtype != MLA_DTYPE_BF16 && pool->dtype != MLA_DTYPE_FP8_E4M3) return false;
+  if (pool->dtype == MLA_DTYPE_FP8_E4M3 && !(pool->kv_scale > 0.f)) return false;
+  return aligned(pool->data, 16);
+}
+
+int max_clusters() { return mla::decode_max_active_clusters(); }
+
+}  // namespace
+
+extern "C" {
+
+int mla_kv_write(const mla_kv_pool* pool, int layer, const void* new_rows, const int64_t* slot_mapping,
+                 int n, void* workspace, void* stream) {
+  if (n < 0 || !valid_pool(pool) || layer < 0 || layer >= pool->num_layers) return MLA_ERR_ARG;
+  if (n == 0) return MLA_OK;
+  if (!new_rows || !slot_mapping || !aligned(new_rows, 16)) return MLA_ERR_ARG;
+  int* status = workspace ? &reinterpret_cast<WsHeader*>(workspace)->status : nullptr;
+  const int64_t layer_rows = static_cast<int64_t>(pool->num_pages) * pool->page_size;
+  cudaError_t e = mla::launch_kv_write(pool->data, pool->dtype, layer_rows, layer, pool->kv_scale, new_rows,
+                                       slot_mapping, n, status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_decode_num_clusters(void) {
+  const int c = max_clusters();
+  return c > 0 ? c : MLA_ERR_CUDA;
+}
+
+size_t mla_decode_workspace_size(int batch, int num_heads) {
+  if (batch < 0 || num_heads <= 0 || num_heads > 128) return 0;
+  const int c = max_clusters();
+  if (c <= 0) return 0;
+  return mla::ws_layout(batch, num_heads, c).total;
+}
+
+int mla_decode_plan(const int32_t* context_lens, int batch, int num_heads, int page_size, int window,
+                    int num_clusters, void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch < 0 || window < 0 || num_clusters < 0 || !workspace) return MLA_ERR_ARG;
+  if (batch > 0 && !context_lens) return MLA_ERR_ARG;
+  if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return MLA_ERR_UNSUPPORTED;
+  const int cmax = max_clusters();
+  if (cmax <= 0) return MLA_ERR_CUDA;
+  const WsLayout lay = mla::ws_layout(batch, num_heads, cmax);
+  if (!aligned(workspace, 256) || workspace_bytes < lay.total) return MLA_ERR_WORKSPACE;
+  const int c = (num_clusters == 0 || num_clusters > cmax) ? cmax : num_clusters;
+  cudaError_t e = mla::launch_plan(context_lens, batch, num_heads, page_size, window, c,
+                                   static_cast<uint8_t*>(workspace), lay, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t* page_indptr,
+               const int32_t* page_ids, int max_blocks, const int32_t* context_lens, int batch, int num_heads,
+               float softmax_scale, int window, void* workspace, void* out, float* lse, void* stream) {
+  if (!valid_pool(pool) || layer < 0 || layer >= pool->num_layers || batch < 0 || window < 0 || !workspace)
+    return MLA_ERR_ARG;
+  if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
+  if (pool->dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED;
+  if (batch == 0) return MLA_OK;
+  if (!q || !page_ids || !context_lens || !out || !aligned(q, 16) || !aligned(out, 16)) return MLA_ERR_ARG;
+  if (!page_indptr && max_blocks <= 0) return MLA_ERR_ARG;
+  if (!(softmax_scale > 0.f)) return MLA_ERR_ARG;
+  const int cmax = max_clusters();
+  if (cmax <= 0) return MLA_ERR_CUDA;
+  if (!aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
+
+  const int ps = pool->page_size;
+  const uint64_t total_rows = static_cast<uint64_t>(pool->num_layers) * pool->num_pages * ps;
+  if (total_rows >= (1ull << 31)) return MLA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+  CUtensorMap kv_map, q_map;
+  if (!make_map_2d(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->data, total_rows, mla::kDimRow,
+                   mla::kDimRow * 2, 64, ps < 64 ? ps : 64))
+    return MLA_ERR_CUDA;
+  if (!make_map_2d(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, static_cast<uint64_t>(batch) * num_heads,
+                   mla::kDimRow, mla::kDimRow * 2, 64, 128))
+    return MLA_ERR_CUDA;
+
+  mla::DecodeArgs a;
+  memset(&a, 0, sizeof a);
+  a.page_indptr = page_indptr;
+  a.page_ids = page_ids;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.lse = lse;
+  a.ws = static_cast<uint8_t*>(workspace);
+  a.lay = mla::ws_layout(batch, num_heads, cmax);
+  a.max_blocks = max_blocks;
+  a.batch = batch;
+  a.num_heads = num_heads;
+  a.page_size = ps;
+  a.window = window;
+  a.num_pages = pool->num_pages;
+  a.num_layers = pool->num_layers;
+  a.layer = layer;
+  a.dtype = pool->dtype;
+  a.kv_scale = pool->kv_scale;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = mla::launch_decode(kv_map, q_map, a, cmax, st);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  e = mla::launch_merge(a, st);
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_uv_project(const void* attn_out, const void* w_uv, void* y, int batch, int num_heads, void* stream) {
+  if (batch < 0 || num_heads <= 0) return MLA_ERR_ARG;
+  if (batch == 0) return MLA_OK;
+  if (!attn_out || !w_uv || !y || !aligned(attn_out, 16) || !aligned(w_uv, 16) || !aligned(y, 16))
+    return MLA_ERR_ARG;
+  auto fn = encode_fn();
+  if (!fn) return MLA_ERR_CUDA;
+  CUtensorMap a_map, w_map;
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(mla::kDimCkv), static_cast<cuuint64_t>(num_heads),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {mla::kDimCkv * 2ull, static_cast<cuuint64_t>(num_heads) * mla::kDimCkv * 2ull};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&a_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(attn_out), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLA_ERR_CUDA;
+  }
+  if (!make_map_2d(&w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_uv, static_cast<uint64_t>(num_heads) * mla::kDimCkv,
+                   mla::kDimV, mla::kDimV * 2, 64, 64))
+    return MLA_ERR_CUDA;
+  cudaError_t e = mla::launch_uv_project(a_map, w_map, y, batch, num_heads, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_get_error(void* workspace, int* code, int clear, void* stream) {
+  if (!workspace || !code) return MLA_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  *code = v;
+  if (clear) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,119 @@
+// Internal layout shared by the host entry points and the kernels: the
+// decode workspace, the work-item record the planner writes, and the
+// launcher prototypes of each kernel file.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mla {
+
+constexpr int kDimCkv = 512;
+constexpr int kDimRope = 64;
+constexpr int kDimRow = 576;
+constexpr int kDimV = 128;
+constexpr int kBlockTokens = 64;  // tokens per schedule block = per decode tile
+
+// One contiguous run of 64-token blocks of one request, processed by one
+// cluster. Attended positions of the item are [tok_lo, tok_hi).
+struct WorkItem {
+  int b;
+  int blk_begin;
+  int blk_end;   // exclusive
+  int slot;      // -1: whole request, write the final output; else partial index
+  int tok_lo;
+  int tok_hi;
+  int cluster;
+  int pad;
+};
+
+struct SplitRequest {
+  int b;
+  int num_splits;
+  int first_partial;
+  int pad;
+};
+
+struct WsHeader {
+  int status;  // sticky MLA_STATUS_* bits
+  int batch;
+  int num_heads;
+  int page_size;
+  int window;
+  int num_clusters;   // clusters the plan spread work over (<= requested)
+  int total_blocks;
+  int num_items;
+  int num_partials;
+  int num_split;
+  int planned;        // 1 after a successful plan
+  int pad[5];
+};
+
+struct WsLayout {
+  size_t items, cluster_start, split, req_scratch, partial_lse, partial_o, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Byte offsets of each region for (batch, heads, clusters).
+__host__ __device__ inline WsLayout ws_layout(int batch, int heads, int clusters) {
+  WsLayout L;
+  size_t off = align_up(sizeof(WsHeader), 256);
+  L.items = off;
+  off = align_up(off + sizeof(WorkItem) * static_cast<size_t>(batch + clusters), 256);
+  L.cluster_start = off;
+  off = align_up(off + sizeof(int) * static_cast<size_t>(clusters + 1), 256);
+  L.split = off;
+  off = align_up(off + sizeof(SplitRequest) * static_cast<size_t>(batch), 256);
+  L.req_scratch = off;
+  off = align_up(off + sizeof(int) * 4 * static_cast<size_t>(batch), 256);
+  const size_t max_partials = 2 * static_cast<size_t>(clusters);
+  L.partial_lse = off;
+  off = align_up(off + sizeof(float) * max_partials * heads, 256);
+  L.partial_o = off;
+  off = align_up(off + sizeof(float) * max_partials * heads * kDimCkv, 256);
+  L.total = off;
+  return L;
+}
+
+struct DecodeArgs {
+  const int32_t* page_indptr;
+  const int32_t* page_ids;
+  const int32_t* context_lens;
+  void* out;        // bf16 [B][H][512]
+  float* lse;       // [B][H] or null
+  uint8_t* ws;
+  WsLayout lay;
+  int max_blocks;
+  int batch;
+  int num_heads;
+  int page_size;
+  int window;
+  int num_pages;
+  int num_layers;
+  int layer;
+  int dtype;
+  float kv_scale;
+  float scale_log2;  // softmax_scale * log2(e)
+};
+
+// kv_write.cu
+cudaError_t launch_kv_write(void* pool, int dtype, int64_t layer_rows, int layer, float kv_scale,
+                            const void* rows, const int64_t* slots, int n, int* status,
+                            cudaStream_t stream);
+// plan_merge.cu
+cudaError_t launch_plan(const int32_t* context_lens, int batch, int heads, int page_size,
+                        int window, int clusters, uint8_t* ws, const WsLayout& lay,
+                        cudaStream_t stream);
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream);
+// decode_sm103.cu
+cudaError_t launch_decode(const CUtensorMap& kv_map, const CUtensorMap& q_map, const DecodeArgs& a,
+                          int clusters, cudaStream_t stream);
+int decode_max_active_clusters();
+// uv_project.cu
+cudaError_t launch_uv_project(const CUtensorMap& a_map, const CUtensorMap& w_map, void* y,
+                              int batch, int heads, cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,248 @@
+// Split-KV schedule and partial-result merge.
+//
+// The plan runs on the device so that it can be captured with the decode
+// and so that a replay reads exactly the buffer the last plan filled (the
+// plan/run contract described in SGLang PR #32972 "Let Kimi-Linear use the
+// paged MLA attention backends", Correction). It reads only the lengths:
+// request b attends positions [s_b, L_b] (s_b = 0, or max(0, L_b + 1 - W)
+// for a sliding window, FastDeploy PR #8049 "Support MLA_SWA
+// functionality"), i.e. 64-token blocks s_b/64 .. L_b/64. The blocks of all
+// requests, concatenated in request order, are cut into C equal contiguous
+// ranges, one per cluster; a request crossing a range boundary becomes
+// several items whose partial (O, lse) are merged afterwards.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "../../include/mla_decode.h"
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// Block-wide exclusive scan of one int per thread; returns the prefix and
+// writes the block total to *total.
+__device__ int block_excl_scan(int v, int* total, int* smem32) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) smem32[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = smem32[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    smem32[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int warp_prefix = warp ? smem32[warp - 1] : 0;
+  *total = smem32[31];
+  __syncthreads();
+  return warp_prefix + x - v;
+}
+
+__device__ __forceinline__ long long range_lo(long long c, long long T, long long C) {
+  return c * T / C;
+}
+
+// Cluster whose range [lo(c), lo(c+1)) holds block x (requires T >= C).
+__device__ __forceinline__ int cluster_of(long long x, long long T, long long C) {
+  return static_cast<int>(((x + 1) * C + T - 1) / T - 1);
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+    plan_kernel(const int32_t* __restrict__ lens, int B, int H, int ps, int window, int C_req,
+                uint8_t* __restrict__ ws, WsLayout lay) {
+  __shared__ int smem32[32];
+  __shared__ int bad_len;
+  WsHeader* hd = reinterpret_cast<WsHeader*>(ws);
+  int* req = reinterpret_cast<int*>(ws + lay.req_scratch);  // [B][4]: first_blk, n_blk, off, start
+  WorkItem* items = reinterpret_cast<WorkItem*>(ws + lay.items);
+  int* cstart = reinterpret_cast<int*>(ws + lay.cluster_start);
+  SplitRequest* split = reinterpret_cast<SplitRequest*>(ws + lay.split);
+  const int tid = threadIdx.x;
+  if (tid == 0) bad_len = 0;
+  __syncthreads();
+
+  // Pass 1: blocks per request and their offsets in the concatenated order.
+  long long T = 0;
+  for (int base = 0; base < B; base += kPlanThreads) {
+    const int i = base + tid;
+    int n = 0;
+    if (i < B) {
+      int L = lens[i];
+      if (L < 0) {
+        bad_len = 1;
+        L = 0;
+      }
+      const int s = window > 0 ? max(0, L + 1 - window) : 0;
+      const int first = s / kBlockTokens;
+      n = L / kBlockTokens - first + 1;
+      req[4 * i + 0] = first;
+      req[4 * i + 1] = n;
+      req[4 * i + 3] = s;
+    }
+    int chunk_total;
+    const int ex = block_excl_scan(n, &chunk_total, smem32);
+    if (i < B) req[4 * i + 2] = static_cast<int>(T) + ex;
+    T += chunk_total;
+  }
+  __syncthreads();
+  const long long C = T > 0 ? (T < C_req ? T : C_req) : 1;
+
+  // Pass 2: one item per (request, cluster range it meets), in request order,
+  // which is also cluster order.
+  int n_items = 0, n_part = 0, n_split = 0;
+  for (int base = 0; base < B; base += kPlanThreads) {
+    const int i = base + tid;
+    int ns = 0, first = 0, n = 0, off = 0, s = 0, cf = 0;
+    if (i < B) {
+      first = req[4 * i + 0];
+      n = req[4 * i + 1];
+      off = req[4 * i + 2];
+      s = req[4 * i + 3];
+      cf = cluster_of(off, T, C);
+      const int cl = cluster_of(static_cast<long long>(off) + n - 1, T, C);
+      ns = cl - cf + 1;
+    }
+    int t_items, t_part, t_split;
+    const int ex_items = block_excl_scan(ns, &t_items, smem32);
+    const int ex_part = block_excl_scan(ns > 1 ? ns : 0, &t_part, smem32);
+    const int ex_split = block_excl_scan(ns > 1 ? 1 : 0, &t_split, smem32);
+    if (i < B) {
+      int L = lens[i];
+      if (L < 0) L = 0;
+      const int item0 = n_items + ex_items;
+      const int part0 = n_part + ex_part;
+      for (int k = 0; k < ns; ++k) {
+        const int c = cf + k;
+        const long long lo = max(static_cast<long long>(off), range_lo(c, T, C));
+        const long long hi = min(static_cast<long long>(off) + n, range_lo(c + 1, T, C));
+        WorkItem w;
+        w.b = i;
+        w.blk_begin = first + static_cast<int>(lo - off);
+        w.blk_end = first + static_cast<int>(hi - off);
+        w.slot = ns > 1 ? part0 + k : -1;
+        w.tok_lo = s;
+        w.tok_hi = L + 1;
+        w.cluster = c;
+        w.pad = 0;
+        items[item0 + k] = w;
+      }
+      if (ns > 1) {
+        SplitRequest r;
+        r.b = i;
+        r.num_splits = ns;
+        r.first_partial = part0;
+        r.pad = 0;
+        split[n_split + ex_split] = r;
+      }
+    }
+    n_items += t_items;
+    n_part += t_part;
+    n_split += t_split;
+  }
+  __syncthreads();
+
+  // Pass 3: first item of each cluster (items are sorted by cluster).
+  for (int c = tid; c <= C_req; c += kPlanThreads) {
+    int lo = 0, hi = n_items;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (items[mid].cluster < c) lo = mid + 1;
+      else hi = mid;
+    }
+    cstart[c] = lo;
+  }
+  if (tid == 0) {
+    if (bad_len) atomicOr(&hd->status, MLA_STATUS_BAD_LENGTH);
+    hd->batch = B;
+    hd->num_heads = H;
+    hd->page_size = ps;
+    hd->window = window;
+    hd->num_clusters = static_cast<int>(C);
+    hd->total_blocks = static_cast<int>(T);
+    hd->num_items = n_items;
+    hd->num_partials = n_part;
+    hd->num_split = n_split;
+    hd->planned = 1;
+  }
+}
+
+constexpr int kMergeHeadsPerBlock = 4;
+
+// out[b,h] = sum_s 2^(lse_s - m) O_s / sum_s 2^(lse_s - m), O_s normalised
+// per split, lse in log2 units; the natural-log lse is reported.
+__global__ void __launch_bounds__(32 * kMergeHeadsPerBlock)
+    merge_kernel(const uint8_t* __restrict__ ws, WsLayout lay, int H,
+                 __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
+  const WsHeader* hd = reinterpret_cast<const WsHeader*>(ws);
+  if (static_cast<int>(blockIdx.x) >= hd->num_split) return;
+  const SplitRequest sr = reinterpret_cast<const SplitRequest*>(ws + lay.split)[blockIdx.x];
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kMergeHeadsPerBlock + (threadIdx.x >> 5);
+  if (h >= H) return;
+  const float* plse = reinterpret_cast<const float*>(ws + lay.partial_lse);
+  const float* po = reinterpret_cast<const float*>(ws + lay.partial_o);
+  float m = -CUDART_INF_F;
+  for (int s = 0; s < sr.num_splits; ++s) m = fmaxf(m, plse[(sr.first_partial + s) * H + h]);
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  for (int s = 0; s < sr.num_splits; ++s) {
+    const int p = sr.first_partial + s;
+    const float w = exp2f(plse[p * H + h] - m);
+    wsum += w;
+    const float4* src = reinterpret_cast<const float4*>(po + (static_cast<size_t>(p) * H + h) * kDimCkv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 v = src[lane + 32 * j];
+      acc[j].x += w * v.x;
+      acc[j].y += w * v.y;
+      acc[j].z += w * v.z;
+      acc[j].w += w * v.w;
+    }
+  }
+  const float inv = 1.f / wsum;
+  __nv_bfloat16* dst = out + (static_cast<size_t>(sr.b) * H + h) * kDimCkv;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst + 4 * (lane + 32 * j)) = pk;
+  }
+  if (lse_out && lane == 0)
+    lse_out[static_cast<size_t>(sr.b) * H + h] = (m + log2f(wsum)) * 0.69314718055994531f;
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* context_lens, int batch, int heads, int page_size,
+                        int window, int clusters, uint8_t* ws, const WsLayout& lay,
+                        cudaStream_t stream) {
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(context_lens, batch, heads, page_size, window,
+                                              clusters, ws, lay);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.batch <= 0) return cudaSuccess;
+  const dim3 grid(a.batch, (a.num_heads + kMergeHeadsPerBlock - 1) / kMergeHeadsPerBlock);
+  merge_kernel<<<grid, 32 * kMergeHeadsPerBlock, 0, stream>>>(
+      a.ws, a.lay, a.num_heads, static_cast<__nv_bfloat16*>(a.out), a.lse);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

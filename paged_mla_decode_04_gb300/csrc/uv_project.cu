@@ -1,0 +1,137 @@
+// W_UV projection after latent attention: y[b,h,:] = attn_out[b,h,:] W_UV[h]
+// (v_head_dim 128 of MoE-Infinity PR #195 "DeepSeek-V2/V3 paged-attention
+// shim (MLA)", Root causes 3). Per head a [B x 512] x [512 x 128] GEMM.
+//
+// One CTA per (head, 128 requests): TMA stages 64-wide K chunks of the
+// attention output (K-major A) and of W_UV (N contiguous, MN-major B) in a
+// 4-stage ring; one thread issues tcgen05.mma M=128 N=128 K=16 into a
+// 128-column TMEM accumulator; four warps read it back (one TMEM lane per
+// request row) and store bf16.
+#include <cuda_bf16.h>
+
+#include "../../include/mla_decode.h"
+#include "mla_internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kKChunks = kDimCkv / 64;        // 8
+constexpr int kABytes = 128 * 128;            // [128 rows][64 k] bf16
+constexpr int kWBytes = 64 * 128;             // [64 k][64 n] bf16
+constexpr int kStageBytes = kABytes + 2 * kWBytes;
+constexpr int kOffBar = kStages * kStageBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;
+constexpr int kThreads = 128;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    uv_project_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap w_map,
+                      __nv_bfloat16* __restrict__ y, int B, int H) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bar0 = sbase + kOffBar;
+  auto full = [&](int s) -> uint32_t { return bar0 + 8u * s; };
+  auto empty = [&](int s) -> uint32_t { return bar0 + 8u * (kStages + s); };
+  const uint32_t done = bar0 + 8u * (2 * kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (2 * kStages + 1));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x;
+  const int b0 = blockIdx.y * 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    for (int kc = 0; kc < kKChunks; ++kc) {
+      const int s = kc % kStages, use = kc / kStages;
+      if (!mbar_wait(empty(s), (use & 1) ^ 1, nullptr)) break;
+      mbar_arrive_expect_tx(full(s), kStageBytes);
+      const uint32_t dst = sbase + s * kStageBytes;
+      tma_load_3d(dst, &a_map, full(s), kc * 64, h, b0);
+      tma_load_2d(dst + kABytes, &w_map, full(s), 0, h * kDimCkv + kc * 64);
+      tma_load_2d(dst + kABytes + kWBytes, &w_map, full(s), 64, h * kDimCkv + kc * 64);
+    }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = idesc_bf16(128, 128, false, true);
+    for (int kc = 0; kc < kKChunks; ++kc) {
+      const int s = kc % kStages, use = kc / kStages;
+      if (!mbar_wait(full(s), use & 1, nullptr)) break;
+      tc_fence_after();
+      const uint32_t st = sbase + s * kStageBytes;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t ad = sdesc_sw128(st + k * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(st + kABytes + k * 16 * 128, kWBytes, 1024);
+        mma_bf16_ss(tmem, ad, bd, idesc, (kc | k) != 0);
+      }
+      mma_commit(empty(s));
+    }
+    mma_commit(done);
+  }
+  __syncwarp();
+  // Every thread waits for the accumulator (bounded), then reads its row.
+  const bool ready = __all_sync(0xffffffffu, mbar_wait(done, 0, nullptr));
+  tc_fence_after();
+  const int row = warp * 32 + lane;
+  const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  if (ready) {
+#pragma unroll 1
+    for (int c = 0; c < 128 / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld16(taddr + c * 32, r);
+      tmem_ld16(taddr + c * 32 + 16, r + 16);
+      tmem_wait_ld();
+      if (b0 + row < B) {
+        __nv_bfloat16* dst = y + (static_cast<size_t>(b0 + row) * H + h) * kDimV + c * 32;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 pk;
+          pk.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+          pk.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+          pk.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+          pk.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+          reinterpret_cast<uint4*>(dst)[v] = pk;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 128);
+}
+
+}  // namespace
+
+cudaError_t launch_uv_project(const CUtensorMap& a_map, const CUtensorMap& w_map, void* y, int batch,
+                              int heads, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(uv_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const dim3 grid(heads, (batch + 127) / 128);
+  uv_project_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a_map, w_map, static_cast<__nv_bfloat16*>(y),
+                                                            batch, heads);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,250 @@
+"""GPU parity: the library's CUDA path against the CPU oracle, element by
+element, on seeded workloads. Latent writes are compared bit-exact over the
+whole pool; attention outputs within max|gpu - ref| <= 1e-2 * max|ref| for a
+bf16 cache (fp32 accumulation, bf16 output)."""
+import numpy as np
+import pytest
+import torch
+
+import mla_workloads as mw
+import oracle
+from mla_testlib import (TOL_BF16, DeviceWorkload, bf16_tensor, f64, oracle_pool_after_write,
+                         oracle_step, rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import paged_mla_decode_04_gb300 as m
+    m.load_library()
+    return m
+
+
+def _check(gpu_out, gpu_lse, ref_out, ref_lse, tol=TOL_BF16):
+    err = rel_err(gpu_out, ref_out)
+    assert err <= tol, "out rel err %.3e" % err
+    lerr = np.abs(gpu_lse - ref_lse).max()
+    assert lerr <= 2e-3 * max(1.0, np.abs(ref_lse).max()), "lse err %.3e" % lerr
+    return err
+
+
+# ----------------------------------------------------------------- latent write
+
+@pytest.mark.parametrize("name", ["tiny", "v2lite"])
+def test_kv_write_bf16_bit_exact_whole_pool(lib, name):
+    wl = mw.make(name, batch=8 if name != "tiny" else None)
+    dw = DeviceWorkload(wl, lib)
+    slots = wl.slot_mapping.copy()
+    slots[0] = -1                                        # pad row
+    lib.kv_write(dw.pool, wl.layer, dw.new_rows, torch.from_numpy(slots).cuda(), dw.ws)
+    torch.cuda.synchronize()
+    ref = wl.pool_bf16.copy()
+    oracle.kv_write(ref, mw.BF16, wl.num_layers, wl.num_pages, wl.page_size, 1.0, wl.layer,
+                    wl.new_rows, slots)
+    got = dw.pool.data.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+    assert lib.get_error(dw.ws) == 0
+
+
+def test_kv_write_fp8_bit_exact_whole_pool(lib):
+    wl = mw.make("fp8", batch=3, context_lens=[100, 5, 260], page_size=64)
+    dw = DeviceWorkload(wl, lib)             # fills every row through the GPU write
+    lib.kv_write(dw.pool, wl.layer, dw.new_rows, dw.slots, dw.ws)
+    torch.cuda.synchronize()
+    ref = oracle_pool_after_write(wl)
+    got = dw.pool.data.cpu().numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_kv_write_out_of_range_slot_sets_status_and_skips(lib):
+    wl = mw.make("tiny")
+    dw = DeviceWorkload(wl, lib)
+    before = dw.pool.data.clone()
+    bad = torch.tensor([wl.num_pages * wl.page_size, -5], dtype=torch.int64, device="cuda")
+    lib.kv_write(dw.pool, 0, dw.new_rows, bad, dw.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(before, dw.pool.data)
+    assert lib.get_error(dw.ws, clear=True) & lib.STATUS_BAD_SLOT
+    assert lib.get_error(dw.ws) == 0
+
+
+# ----------------------------------------------------------------- decode
+
+def test_tiny_config_both_layers_csr_and_table(lib):
+    wl = mw.make("tiny")
+    for layer in (0, 1):
+        dw = DeviceWorkload(wl, lib)
+        for csr in (False, True):
+            out, lse = dw.step(layer=layer, csr=csr, write=not csr)
+            ref_out, ref_lse = oracle_step(wl, layer=layer)
+            _check(out, lse, ref_out, ref_lse)
+        assert lib.get_error(dw.ws) == 0
+
+
+def test_tiny_config_matches_unabsorbed_mha_form(lib):
+    """GPU absorbed decode + W_UV projection against the oracle's unabsorbed
+    192/128-dim multi-head form (q_abs rounded to bf16 for the GPU)."""
+    wl = mw.make("tiny")
+    e = wl.extra
+    q_abs = oracle.absorb_query(e["q_nope"], e["q_rope"], e["w_uk"])
+    wl.q = mw.f32_to_bf16_bits(q_abs.astype(np.float32))
+    dw = DeviceWorkload(wl, lib)
+    out, _ = dw.step()
+    w_uv = mw.f32_to_bf16_bits(e["w_uv"].astype(np.float32))
+    y = torch.empty(wl.batch, wl.num_heads, 128, dtype=torch.bfloat16, device="cuda")
+    lib.uv_project(dw.out, bf16_tensor(w_uv), y)
+    torch.cuda.synchronize()
+    pool = oracle_pool_after_write(wl)
+    y_ref = oracle.decode_unabsorbed(pool, mw.BF16, wl.num_layers, wl.num_pages, wl.page_size,
+                                     1.0, wl.layer, e["q_nope"], e["q_rope"], e["w_uk"],
+                                     oracle.bf16_bits_to_f64(w_uv), wl.context_lens,
+                                     wl.softmax_scale, block_table=wl.block_table)
+    assert rel_err(f64(y), y_ref) <= 2e-2
+
+
+@pytest.mark.parametrize("heads", [16, 32, 64, 128])
+@pytest.mark.parametrize("ps", [16, 32, 64, 128])
+def test_ragged_lengths_heads_and_page_sizes(lib, heads, ps):
+    lens = [0, 1, 63, 64, 65, 200, 777]
+    wl = mw.make("v3", num_heads=heads, context_lens=lens, page_size=ps)
+    dw = DeviceWorkload(wl, lib)
+    out, lse = dw.step()
+    ref_out, ref_lse = oracle_step(wl)
+    _check(out, lse, ref_out, ref_lse)
+    assert lib.get_error(dw.ws) == 0
+
+
+@pytest.mark.parametrize("window", [1, 5, 64, 100, 4096])
+def test_sliding_window(lib, window):
+    lens = [0, 30, 64, 129, 700, 1500]
+    wl = mw.make("long_window", context_lens=lens, window=window)
+    dw = DeviceWorkload(wl, lib)
+    out, lse = dw.step()
+    ref_out, ref_lse = oracle_step(wl)
+    _check(out, lse, ref_out, ref_lse)
+
+
+def test_window_covering_everything_equals_full(lib):
+    lens = [10, 300, 999]
+    wl = mw.make("long_window", context_lens=lens, window=1000)
+    dw = DeviceWorkload(wl, lib)
+    win, _ = dw.step(window=1000)
+    full, _ = dw.step(window=0, write=False)
+    assert np.array_equal(win, full)
+
+
+@pytest.mark.parametrize("clusters", [1, 2, 7, 0])
+def test_split_count_invariance(lib, clusters):
+    lens = [3000, 17, 900, 2500]
+    wl = mw.make("v3", context_lens=lens)
+    dw = DeviceWorkload(wl, lib)
+    ref_out, ref_lse = oracle_step(wl)
+    out, lse = dw.step(num_clusters=clusters)
+    _check(out, lse, ref_out, ref_lse)
+    base, _ = dw.step(num_clusters=1, write=False)
+    assert rel_err(out, base) <= 5e-3
+
+
+def test_page_permutation_is_bit_identical(lib):
+    wl = mw.make("v2lite", batch=6)
+    dw = DeviceWorkload(wl, lib)
+    out, lse = dw.step()
+    rng = np.random.default_rng(11)
+    perm = rng.permutation(wl.num_pages)
+    wl2 = mw.make("v2lite", batch=6)
+    wl2.pool_bf16 = np.empty_like(wl.pool_bf16)
+    wl2.pool_bf16[:, perm] = wl.pool_bf16
+    wl2.block_table = np.where(wl.block_table >= 0, perm[np.maximum(wl.block_table, 0)], -1).astype(
+        np.int32)
+    wl2.page_ids = perm[wl.page_ids].astype(np.int32)
+    wl2.slot_mapping = np.array([wl2.block_table[b, L // wl.page_size] * wl.page_size +
+                                 L % wl.page_size for b, L in enumerate(wl.context_lens.tolist())],
+                                np.int64)
+    dw2 = DeviceWorkload(wl2, lib)
+    out2, lse2 = dw2.step()
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_needle_sweep_pins_indexing_bit_exact(lib):
+    """q_rope = c e_j, k_rope[t*] = e_j only: the softmax collapses on t*, so
+    the output is c_kv[t*] exactly (bf16 in, bf16 out) for every position,
+    across page boundaries, a window edge and the new-token slot."""
+    lens = [150, 70]
+    wl = mw.make("tiny", num_heads=16, context_lens=lens, page_size=16)
+    j, c = 7, 2048.0
+    wl.q[:] = 0
+    wl.q[:, :, 512 + j] = mw.f32_to_bf16_bits(np.float32([c]))[0]
+    pool0 = wl.pool_bf16.copy()
+    pool0[:, :, :, 512 + j] = 0
+    wl.new_rows[:, 512 + j] = 0
+    one = mw.f32_to_bf16_bits(np.float32([1.0]))[0]
+    for window in (0, 40):
+        for b, L in enumerate(lens):
+            start = max(0, L + 1 - window) if window else 0
+            for t_star in range(start, L):      # position L is the new token
+                wl.pool_bf16 = pool0.copy()
+                wl.pool_bf16[wl.layer, wl.block_table[b, t_star // 16], t_star % 16, 512 + j] = one
+                dw = DeviceWorkload(wl, lib)
+                out, _ = dw.step(window=window)
+                row = oracle.bf16_bits_to_f64(
+                    wl.pool_bf16[wl.layer, wl.block_table[b, t_star // 16], t_star % 16])
+                np.testing.assert_array_equal(out[b], np.broadcast_to(row[:512], out[b].shape))
+
+
+def test_layers_do_not_alias(lib):
+    wl = mw.make("tiny")
+    dw = DeviceWorkload(wl, lib)
+    out1, _ = dw.step(layer=1)
+    dw.pool.data[0].fill_(3.0)
+    lib.kv_write(dw.pool, 0, dw.new_rows, dw.slots, dw.ws)
+    out1b, _ = dw.step(layer=1, write=False)
+    assert np.array_equal(out1, out1b)
+
+
+def test_bad_page_id_sets_status_without_fault(lib):
+    wl = mw.make("tiny")
+    wl.block_table[0, 1] = wl.num_pages + 5
+    dw = DeviceWorkload(wl, lib)
+    dw.step(write=False)
+    assert lib.get_error(dw.ws) & lib.STATUS_BAD_PAGE
+
+
+def test_plan_mismatch_sets_status(lib):
+    wl = mw.make("tiny")
+    dw = DeviceWorkload(wl, lib)
+    lib.plan(dw.lens, wl.num_heads, wl.page_size, 0, dw.ws)
+    lib.decode(dw.pool, 1, dw.q, dw.lens, wl.softmax_scale, dw.ws, dw.out,
+               block_table=dw.block_table, window=7)
+    torch.cuda.synchronize()
+    assert lib.get_error(dw.ws) & lib.STATUS_PLAN_MISMATCH
+
+
+# ----------------------------------------------------------------- W_UV
+
+@pytest.mark.parametrize("batch,heads", [(2, 16), (128, 128), (130, 32)])
+def test_uv_project(lib, batch, heads):
+    rng = np.random.default_rng(batch + heads)
+    a = mw.f32_to_bf16_bits(rng.standard_normal((batch, heads, 512)).astype(np.float32) * 0.1)
+    w = mw.f32_to_bf16_bits(rng.standard_normal((heads, 512, 128)).astype(np.float32) * 0.02)
+    y = torch.empty(batch, heads, 128, dtype=torch.bfloat16, device="cuda")
+    lib.uv_project(bf16_tensor(a), bf16_tensor(w), y)
+    torch.cuda.synchronize()
+    ref = oracle.uv_project(oracle.bf16_bits_to_f64(a), oracle.bf16_bits_to_f64(w))
+    assert rel_err(f64(y), ref) <= TOL_BF16
+
+
+# ----------------------------------------------------------------- full-size configs
+
+@pytest.mark.parametrize("name,sample", [("v2lite", [0, 17, 63]), ("v3", [0, 64, 127]),
+                                         ("long_window", [0, 3, 7]), ("long", [5])])
+def test_full_size_config_sampled(lib, name, sample):
+    """Full batch and lengths in the schedule the bench uses (all clusters);
+    the oracle checks a sample of requests."""
+    wl = mw.make(name)
+    dw = DeviceWorkload(wl, lib)
+    out, lse = dw.step()
+    ref_out, ref_lse = oracle_step(wl, requests=sample)
+    _check(out[sample], lse[sample], ref_out, ref_lse)
+    assert lib.get_error(dw.ws) == 0
+    assert np.isfinite(out).all()
