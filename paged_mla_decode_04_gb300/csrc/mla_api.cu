@@ -119,14 +119,15 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   if (total_rows >= (1ull << 31)) return MLA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
   CUtensorMap kv_map, q_map;
   if (!make_map_2d(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->data, total_rows, mla::kDimRow,
-                   mla::kDimRow * 2, 64, ps < 64 ? ps : 64))
+                   mla::kDimRow * 2, 64, ps < mla::kBlockTokens ? ps : mla::kBlockTokens))
     return MLA_ERR_CUDA;
   if (!make_map_2d(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, static_cast<uint64_t>(batch) * num_heads,
-                   mla::kDimRow, mla::kDimRow * 2, 64, 128))
+                   mla::kDimRow, mla::kDimRow * 2, 64, 64))
     return MLA_ERR_CUDA;
 
   mla::DecodeArgs a;
   memset(&a, 0, sizeof a);
+  a.pool = pool->data;
   a.page_indptr = page_indptr;
   a.page_ids = page_ids;
   a.context_lens = context_lens;

@@ -14,9 +14,9 @@ constexpr int kDimCkv = 512;
 constexpr int kDimRope = 64;
 constexpr int kDimRow = 576;
 constexpr int kDimV = 128;
-constexpr int kBlockTokens = 64;  // tokens per schedule block = per decode tile
+constexpr int kBlockTokens = 32;  // tokens per schedule block = per decode tile
 
-// One contiguous run of 64-token blocks of one request, processed by one
+// One contiguous run of 32-token blocks of one request, processed by one
 // cluster. Attended positions of the item are [tok_lo, tok_hi).
 struct WorkItem {
   int b;
@@ -79,6 +79,7 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int heads, int clusters
 }
 
 struct DecodeArgs {
+  const void* pool;  // pool base (bf16 rows), for L2 prefetch
   const int32_t* page_indptr;
   const int32_t* page_ids;
   const int32_t* context_lens;
