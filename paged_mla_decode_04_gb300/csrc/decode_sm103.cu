@@ -9,28 +9,29 @@
 // tokens, contraction 576) and O = P V (heads x 512, contraction over tokens)
 // are dense tensor-core contractions.
 //
-// GB300 mapping. A fp32 O for 128 heads x 512 dims fills a whole SM's tensor
-// memory, so one work unit is a cluster of two CTAs (rank r = 0, 1):
-//   - both ranks gather the full 576-d rows of each 32-token tile by TMA
-//     (one box per page and 64-dim chunk, 128-byte swizzle, 3-stage ring);
-//   - rank r computes S for its half of the heads over all 576 dims with
-//     tcgen05.mma M=64 (heads) x N=32 (tokens) into TMEM, runs the online
-//     softmax for those heads (base 2, lazy rescale: a head's reference max
-//     moves only when its running max grows by more than 8, i.e. a factor
-//     256; the final 1/l makes the result exact) and writes its P rows (bf16)
-//     into its own shared memory and, with st.async, into the peer's;
-//   - rank r accumulates O for all heads but only its half of the value
-//     dims (c_kv[256r, 256r+256)) with tcgen05.mma M=128 x N=256 x K=32,
-//     V read MN-major straight from the gathered tile.
-// Only P rows, rescale factors and final row sums cross between the two SMs
-// (about 136 bytes per token at 128 heads); distributed shared memory is far
-// slower than HBM on this part, so scores never cross.
-// Warp roles per CTA (224 threads): warp 0 TMA producer (which also runs
-// bulk L2 prefetches a few tiles ahead, each rank fetching half of every
-// tile, so HBM latency is hidden beyond what the shared-memory ring holds),
-// warp 1 TMEM owner and QK issuer, warps 2-5 softmax, O correction and
-// epilogue, warp 6 PV issuer (separate issuers, so a QK waiting for data
-// never holds back a PV).
+// GB300 mapping (measured constraints: a fp32 O for 128 heads x 512 dims
+// fills one SM's tensor memory; a tcgen05.mma costs at least ~55 cycles
+// whatever its shape, so only M=128 instructions pay; SM-to-SM shared memory
+// moves ~13 bytes/cycle, well below an SM's share of HBM). One work unit is a
+// cluster of two CTAs, rank r, that split the latent dimension evenly:
+//   - rank r holds c_kv[256r, 256r+256) and rope[32r, 32r+32) of every row
+//     (288 dims) and of q; it gathers its slice of each 64-token tile by TMA
+//     (one box per page and chunk, 3-stage ring) and computes a partial
+//     S_r = Q_r K_r^T for all heads with tcgen05.mma M=128 x N=64 into TMEM;
+//   - the heads are split by TMEM lane quarter: quarter q belongs to rank
+//     q & 1. Each rank sends the partial rows of the other rank's heads with
+//     st.async (fp32, 16 KB per tile), adds the peer's partial to its own
+//     heads, runs their online softmax (base 2, lazy rescale: the reference
+//     max moves only when the running max grows by more than 8, the final
+//     1/l makes the result exact), keeps its P rows in TMEM and sends them
+//     (bf16, with the rescale factor) to the peer, which stores them in its
+//     TMEM too;
+//   - each rank accumulates O for all heads over its 256 value dims with
+//     tcgen05.mma M=128 x N=256 x K=64, P read from TMEM and V read MN-major
+//     straight from the gathered tile.
+// Warp roles per CTA (224 threads): warp 0 TMA producer, warp 1 TMEM owner
+// and QK issuer, warps 2-5 softmax / exchange / correction / epilogue (warp
+// w works on TMEM lane quarter w & 3), warp 6 PV issuer.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -41,30 +42,34 @@
 namespace mla {
 namespace {
 
-constexpr int kTile = kBlockTokens;                 // 32 tokens per tile
+constexpr int kTile = kBlockTokens;                 // 64 tokens per tile
 constexpr int kStages = 3;
-constexpr int kChunks = kDimRow / 64;               // 9 chunks of 64 dims
-constexpr int kKvChunkBytes = kTile * 128;          // [32 tokens][64 dims] bf16
-constexpr int kStageBytes = kChunks * kKvChunkBytes;
-constexpr int kQChunkBytes = 64 * 128;              // [64 heads][64 dims] bf16
-constexpr int kPBytes = 128 * 128;                  // [128 heads][32 tokens] bf16, 128-byte rows
+constexpr int kWideChunks = 4;                      // c_kv chunks of 64 dims per rank
+constexpr int kWideBytes = kTile * 128;             // [64 tokens][64 dims] bf16, 128B swizzle
+constexpr int kNarrowBytes = kTile * 64;            // [64 tokens][32 rope dims], 64B swizzle
+constexpr int kStageBytes = kWideChunks * kWideBytes + kNarrowBytes;   // 36 KB
+constexpr int kQWideBytes = 128 * 128;              // [128 heads][64 dims]
+constexpr int kQNarrowBytes = 128 * 64;             // [128 heads][32 rope dims]
+constexpr int kQBytes = kWideChunks * kQWideBytes + kQNarrowBytes;     // 72 KB
+constexpr int kXBytes = 2 * 32 * kTile * 4;         // partial S of 2 quarters x 32 rows, fp32
+constexpr int kPxBytes = 2 * 32 * kTile * 2;        // P rows of 2 quarters x 32 rows, bf16
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kChunks * kQChunkBytes;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;
-constexpr int kOffAlpha = kOffP + 2 * kPBytes;      // [2][128] fp32 rescale factors
-constexpr int kOffL = kOffAlpha + 2 * 128 * 4;      // [128] fp32 final row sums
-constexpr int kOffBar = kOffL + 128 * 4;
-constexpr int kSmemBytes = kOffBar + 512 + 1024;    // barriers + alignment slack
+constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffX = kOffKV + kStages * kStageBytes;  // [2 buffers]
+constexpr int kOffPx = kOffX + 2 * kXBytes;
+constexpr int kOffPxAlpha = kOffPx + kPxBytes;      // [2 quarters][32] fp32
+constexpr int kOffL = kOffPxAlpha + 256;            // [2 quarters][32] fp32 final row sums
+constexpr int kOffBar = kOffL + 256;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;    // barriers + alignment slack
 constexpr int kThreads = 224;
-constexpr int kPrefetchTiles = 8;  // L2 prefetch distance of the producer, in tiles
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0;                       // O: columns [0, 256), lanes = heads
-constexpr uint32_t kColS = 256;                     // S[b]: columns 256 + 32 b, M=64 layout
+constexpr uint32_t kColO = 0;                       // O: [0, 256)
+constexpr uint32_t kColS = 256;                     // S[b]: 256 + 64 b
+constexpr uint32_t kColP = 384;                     // P[b]: 384 + 32 b (bf16 pairs)
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kPRowBytes = kTile * 2;               // 64 bytes of P per head row
-constexpr int kPeerBytesPerRow = kPRowBytes + 4;    // P row + rescale factor
 
-static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
+static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0 && kOffX % 1024 == 0, "alignment");
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 enum Bar {
   kBarKvFull = 0,                  // [kStages]
@@ -73,19 +78,22 @@ enum Bar {
   kBarQFree,
   kBarSFull,                       // [2]
   kBarSFree = kBarSFull + 2,       // [2]
-  kBarPFull = kBarSFree + 2,       // [2] local arrivals + peer st.async bytes
-  kBarPvDone = kBarPFull + 2,      // [2] PV on that P buffer done in both ranks
-  kBarOFixed = kBarPvDone + 2,     // [2] O rows rescaled for this tile
-  kBarLFull = kBarOFixed + 2,      // final row sums landed
-  kBarDrain,
+  kBarXFull = kBarSFree + 2,       // [2 buffers][2 quarter slots]: peer partial rows landed
+  kBarPxFull = kBarXFull + 4,      // [2 quarter slots]: peer P rows landed
+  kBarOFixed = kBarPxFull + 2,     // [2] P in TMEM and O rescaled for this tile
+  kBarPvDone = kBarOFixed + 2,     // [2] PV on that buffer done in both ranks
+  kBarLFull = kBarPvDone + 2,      // [2 quarter slots] final row sums landed
+  kBarDrain = kBarLFull + 2,
   kBarDrainPv,
   kNumBars
 };
-static_assert(kNumBars * 8 + 16 <= 512, "barrier area");
+static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 
 struct Params {
-  CUtensorMap kv_map;  // pool rows [NL*P*ps][576] bf16, box {64, min(ps, 32)}
-  CUtensorMap q_map;   // q rows [B*H][576] bf16, box {64, 64}
+  CUtensorMap kv_wide;    // pool rows [NL*P*ps][576] bf16, box {64, rows}, 128B swizzle
+  CUtensorMap kv_narrow;  // same rows, box {32, rows}, 64B swizzle
+  CUtensorMap q_wide;     // q rows [B*H][576] bf16, box {64, 128}, 128B swizzle
+  CUtensorMap q_narrow;   // box {32, 128}, 64B swizzle
   DecodeArgs a;
 };
 
@@ -98,6 +106,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  tmem_st16(taddr, r);
+  tmem_st16(taddr + 16, r + 16);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -107,8 +120,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + kNumBars * 8 + 4);
-  const float* alpha_s = reinterpret_cast<const float*>(smem + kOffAlpha);
-  float* l_s = reinterpret_cast<float*>(smem + kOffL);
 
   const DecodeArgs& a = p.a;
   uint8_t* ws = a.ws;
@@ -123,7 +134,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = rank ^ 1u;
   const int cluster_id = blockIdx.x >> 1;
   const int H = a.num_heads;
-  const int Hh = H >> 1;  // heads whose scores this rank computes
   const int ps = a.page_size;
 
   const bool plan_ok = hd->planned == 1 && hd->batch == a.batch && hd->num_heads == a.num_heads &&
@@ -145,11 +155,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarSFree + i), 128);
-      mbar_init(bar(kBarPFull + i), 128);
-      mbar_init(bar(kBarPvDone + i), 2);
+      mbar_init(bar(kBarXFull + 2 * i), 1);
+      mbar_init(bar(kBarXFull + 2 * i + 1), 1);
+      mbar_init(bar(kBarPxFull + i), 1);
       mbar_init(bar(kBarOFixed + i), 128);
+      mbar_init(bar(kBarPvDone + i), 2);
+      mbar_init(bar(kBarLFull + i), 1);
     }
-    mbar_init(bar(kBarLFull), 128);
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarDrainPv), 1);
     *abort_flag = 0;
@@ -160,27 +172,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_map(&p.kv_map);
-    tma_prefetch_map(&p.q_map);
+    tma_prefetch_map(&p.kv_wide);
+    tma_prefetch_map(&p.kv_narrow);
+    tma_prefetch_map(&p.q_wide);
+    tma_prefetch_map(&p.q_narrow);
   }
   tc_fence_before();
-  cluster_sync();  // barriers of both ranks initialised before any remote arrive
+  cluster_sync();  // barriers of both ranks initialised before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int wide_x = 256 * static_cast<int>(rank);        // first c_kv dim of this rank
+  const int narrow_x = 512 + 32 * static_cast<int>(rank);  // first rope dim of this rank
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp walks the tiles; lane 0 issues the copies. Page ids are
     // fetched 32 at a time by the warp (one coalesced load) and handed out
-    // by shuffle, so a tile waits on no global load. A second cursor runs
-    // kPrefetchTiles ahead and pulls this rank's half of each tile's rows
-    // into L2.
+    // by shuffle, so a tile waits on no global load.
     const uint64_t kv_policy = l2_policy_evict_first();
     const int64_t layer_row0 = static_cast<int64_t>(a.layer) * a.num_pages * ps;
     const int oob_row = a.num_layers * a.num_pages * ps;  // reads as zeros
     const int rows_per_box = ps < kTile ? ps : kTile;
     const int boxes = kTile / rows_per_box;
-    const uint8_t* pool_bytes = static_cast<const uint8_t*>(a.pool);
     uint32_t g = 0;
     int last_q_item = -1;
     uint32_t n_items = 0;
@@ -192,51 +205,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int nb = a.page_indptr ? a.page_indptr[w.b + 1] - a.page_indptr[w.b] : a.max_blocks;
       const int32_t* ids = a.page_indptr ? a.page_ids + a.page_indptr[w.b]
                                          : a.page_ids + static_cast<int64_t>(w.b) * a.max_blocks;
-      // Page-id windows of 32 pages: one for the copies, one for prefetches.
-      int batch0 = -64, my_id = -1, pbatch0 = -64, pmy_id = -1;
-      auto page_id = [&](int j, int& b0, int& mine) -> int {
-        if (j - b0 >= 32 || j < b0) {
-          b0 = j;
-          const int jj = j + lane;
-          mine = (jj <= last_page && jj < nb) ? ids[jj] : -1;
-        }
-        return __shfl_sync(0xffffffffu, mine, j - b0);
-      };
-      auto prefetch_tile = [&](int pblk) {
-        if (pblk >= w.blk_end) return;
-        for (int bx = 0; bx < boxes; ++bx) {
-          const int pos0 = pblk * kTile + bx * rows_per_box;
-          const int j = pos0 / ps;
-          if (j < first_page || j > last_page || j >= nb) continue;
-          const int pid = page_id(j, pbatch0, pmy_id);
-          if (lane != 0 || pid < 0 || pid >= a.num_pages) continue;
-          const int64_t row = layer_row0 + static_cast<int64_t>(pid) * ps + pos0 % ps;
-          const uint8_t* src = pool_bytes + row * (kDimRow * 2);
-          const uint32_t bytes = static_cast<uint32_t>(rows_per_box * kDimRow * 2);
-          if (boxes == 1) {  // this rank's half of the tile's contiguous rows
-            prefetch_l2_bulk(src + rank * (bytes / 2), bytes / 2);
-          } else if (bx == static_cast<int>(rank)) {
-            prefetch_l2_bulk(src, bytes);
-          }
-        }
-      };
-      for (int pblk = w.blk_begin; pblk < w.blk_begin + kPrefetchTiles; ++pblk) prefetch_tile(pblk);
+      int batch0 = -64, my_id = -1;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQFree), (n_items & 1u) ^ 1u, abort_flag));
       if (!ok) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kBarQFull), kChunks * kQChunkBytes);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &p.q_map, bar(kBarQFull), c * 64,
-                      w.b * H + static_cast<int>(rank) * Hh);
+        mbar_arrive_expect_tx(bar(kBarQFull), kQBytes);
+        for (int c = 0; c < kWideChunks; ++c)
+          tma_load_2d(sbase + kOffQ + c * kQWideBytes, &p.q_wide, bar(kBarQFull), wide_x + 64 * c, w.b * H);
+        tma_load_2d(sbase + kOffQ + kWideChunks * kQWideBytes, &p.q_narrow, bar(kBarQFull), narrow_x, w.b * H);
       }
       last_q_item = static_cast<int>(n_items);
       for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++g) {
         const uint32_t stage = g % kStages, use = g / kStages;
-        prefetch_tile(blk + kPrefetchTiles);
-        int rows[2];
+        int rows[4];
         int nbox = 0;
 #pragma unroll
-        for (int bx = 0; bx < 2; ++bx) {
+        for (int bx = 0; bx < 4; ++bx) {
           rows[bx] = -1;
           if (bx >= boxes) continue;
           const int pos0 = blk * kTile + bx * rows_per_box;
@@ -247,7 +231,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) flag_status(status, MLA_STATUS_BAD_LENGTH);
             row = oob_row;
           } else {
-            const int pid = page_id(j, batch0, my_id);
+            if (j - batch0 >= 32) {
+              batch0 = j;
+              const int jj = j + lane;
+              my_id = (jj <= last_page && jj < nb) ? ids[jj] : -1;
+            }
+            const int pid = __shfl_sync(0xffffffffu, my_id, j - batch0);
             if (pid < 0 || pid >= a.num_pages) {
               if (lane == 0) flag_status(status, MLA_STATUS_BAD_PAGE);
               row = oob_row;
@@ -262,14 +251,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (lane == 0) {
           const uint32_t kvbar = bar(kBarKvFull + stage);
-          mbar_arrive_expect_tx(kvbar, static_cast<uint32_t>(nbox * kChunks * rows_per_box * 128));
+          mbar_arrive_expect_tx(kvbar, static_cast<uint32_t>(nbox * rows_per_box * (kWideChunks * 128 + 64)));
           const uint32_t dst0 = sbase + kOffKV + stage * kStageBytes;
 #pragma unroll
-          for (int bx = 0; bx < 2; ++bx) {
+          for (int bx = 0; bx < 4; ++bx) {
             if (rows[bx] < 0) continue;
-            for (int c = 0; c < kChunks; ++c)
-              tma_load_2d_hint(dst0 + c * kKvChunkBytes + bx * rows_per_box * 128, &p.kv_map, kvbar, c * 64,
-                               rows[bx], kv_policy);
+            for (int c = 0; c < kWideChunks; ++c)
+              tma_load_2d_hint(dst0 + c * kWideBytes + bx * rows_per_box * 128, &p.kv_wide, kvbar,
+                               wide_x + 64 * c, rows[bx], kv_policy);
+            tma_load_2d_hint(dst0 + kWideChunks * kWideBytes + bx * rows_per_box * 64, &p.kv_narrow, kvbar,
+                             narrow_x, rows[bx], kv_policy);
           }
         }
       }
@@ -289,7 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_bf16(64, kTile, false, false);
+      const uint32_t idesc_qk = idesc_bf16(128, kTile, false, false);
       uint32_t g = 0, n_items = 0;
       bool ok = true;
       for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
@@ -304,14 +295,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar(kBarSFree + b), (u & 1u) ^ 1u, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t kv = sbase + kOffKV + stage * kStageBytes;
-          const uint32_t tS = tmem + kColS + 32u * b;
-          for (int c = 0; c < kChunks; ++c)
+          const uint32_t tS = tmem + kColS + 64u * b;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = sdesc_sw128(sbase + kOffQ + c * kQChunkBytes + k * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(kv + c * kKvChunkBytes + k * 32, 16, 1024);
-              mma_bf16_ss(tS, ad, bd, idesc_qk, (c | k) != 0);
-            }
+          for (int c = 0; c < kWideChunks; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16_ss(tS, sdesc_sw128(sbase + kOffQ + c * kQWideBytes + k * 32, 16, 1024),
+                          sdesc_sw128(kv + c * kWideBytes + k * 32, 16, 1024), idesc_qk, (c | k) != 0);
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            mma_bf16_ss(tS, sdesc_sw64(sbase + kOffQ + kWideChunks * kQWideBytes + k * 32, 512),
+                        sdesc_sw64(kv + kWideChunks * kWideBytes + k * 32, 512), idesc_qk, 1u);
           mma_commit(bar(kBarSFull + b));
         }
         if (ok) mma_commit(bar(kBarQFree));  // every QK of this item issued
@@ -335,17 +329,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int nt = w.blk_end - w.blk_begin;
         for (int t = 0; t < nt; ++t, ++g) {
           const uint32_t b = g & 1u, u = g >> 1;
-          if (!mbar_wait<true>(bar(kBarPFull + b), u & 1u, abort_flag)) { ok = false; break; }
           if (!mbar_wait(bar(kBarOFixed + b), u & 1u, abort_flag)) { ok = false; break; }
           tc_fence_after();
           fence_proxy_async_smem();
-          const uint32_t v0 = sbase + kOffKV + (g % kStages) * kStageBytes + 4 * rank * kKvChunkBytes;
+          const uint32_t v0 = sbase + kOffKV + (g % kStages) * kStageBytes;
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(sbase + kOffP + b * kPBytes + k * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(v0 + k * 16 * 128, kKvChunkBytes, 1024);
-            mma_bf16_ss(tO, ad, bd, idesc_pv, (t | k) != 0);
-          }
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_bf16_ts(tO, tmem + kColP + 32u * b + 8u * k, sdesc_sw128(v0 + k * 16 * 128, kWideBytes, 1024),
+                        idesc_pv, (t | k) != 0);
           mma_commit(bar(kBarKvEmpty + g % kStages));
           mma_commit_both(bar(kBarPvDone + b));
         }
@@ -358,21 +349,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_wait(bar(kBarDrainPv), 0, nullptr);
     }
   } else {
-    // ------------------------------------------------------------ softmax, correction, epilogue
-    // Each S row (one head of this rank) is split over lanes i and i + 16 of
-    // its warp (16 tokens each); every lane also owns O row 32 q4 + lane.
-    // Per tile g: (A) scores -> P in registers; (B) once PV(g-2) is done in
-    // both ranks, P rows go to both ranks' P buffer; (C) once the peer's rows
-    // have landed, rescale the owned O rows and release PV(g).
+    // ------------------------------------------------------------ softmax, exchange, correction, epilogue
+    // This warp works on TMEM lane quarter q4: rows (heads) 32 q4 + lane.
+    // The quarter's softmax belongs to rank q4 & 1 ("own" warp here if that
+    // is this rank); the other rank only holds its partial scores and its
+    // share of O. slot = q4 >> 1 indexes the exchange buffers.
     const int q4 = warp & 3;
-    const int half = lane >> 4;
-    const int srow = q4 * 16 + (lane & 15);
-    const bool s_active = srow < Hh;
-    const int gh = static_cast<int>(rank) * Hh + srow;
-    const int orow = q4 * 32 + lane;
-    const bool o_warp = q4 * 32 < H;
-    const int peer_rows = min(max(Hh - q4 * 16, 0), 16);
-    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const int slot = q4 >> 1;
+    const bool own = static_cast<uint32_t>(q4 & 1) == rank;
+    const int nrow = min(max(H - 32 * q4, 0), 32);  // valid heads in this quarter
+    const int row = 32 * q4 + lane;                 // head of this lane
+    const bool valid = lane < nrow;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
     const uint32_t tO = tmem + lane_base + kColO;
     const uint32_t dim0 = 256u * rank;
     const int tid_sm = threadIdx.x - 64;
@@ -382,34 +370,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto wwait_cluster = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait<true>(b, parity, abort_flag));
     };
-    // Step C for tile gp: rescale owned O rows by the factors both ranks
-    // sent, then let the PV issuer run PV(gp).
-    auto finish_tile = [&](uint32_t gp, bool first_of_item) -> bool {
-      const uint32_t bp = gp & 1u, up = gp >> 1;
-      if (!wwait_cluster(bar(kBarPFull + bp), up & 1u)) return false;
-      if (!first_of_item && o_warp) {
-        const float ao = orow < H ? alpha_s[bp * 128 + orow] : 1.f;
-        if (__any_sync(0xffffffffu, ao != 1.f)) {
-          // O must hold PV(gp - 1) before it is rescaled.
-          if (!wwait(bar(kBarPvDone + ((gp - 1) & 1u)), ((gp - 1) >> 1) & 1u)) return false;
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 256 / 16; ++c) {
-            uint32_t r[16];
-            tmem_ld16(tO + c * 16, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * ao);
-            tmem_st16(tO + c * 16, r);
-          }
-          tmem_wait_st();
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(kBarOFixed + bp));
-      return true;
-    };
+    // Exchange buffers: X[b][slot] holds 32 rows x 64 fp32 as 16 groups of
+    // 4 columns, group-major (lane-contiguous 16-byte pieces); PX[slot] holds
+    // 32 rows x 32 packed bf16 pairs, same arrangement.
+    const uint32_t x_slot0 = sbase + kOffX + slot * (32 * kTile * 4);
+    const uint32_t px_slot = sbase + kOffPx + slot * (32 * kTile * 2);
+    const uint32_t pxa_slot = sbase + kOffPxAlpha + slot * 128;
+    const uint32_t l_slot = sbase + kOffL + slot * 128;
     uint32_t g = 0, n_items = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
@@ -420,140 +387,196 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++g) {
         const int base = blk * kTile;
         const uint32_t b = g & 1u, u = g >> 1;
-        // (A) scores of this tile, 16 per lane.
+        const bool first_tile = blk == w.blk_begin;
+        // Partial scores of this rank for this quarter's rows.
         if (!wwait(bar(kBarSFull + b), u & 1u)) { ok = false; break; }
         tc_fence_after();
-        float s[16];
-        {
-          uint32_t r[16];
-          tmem_ld16x2(tmem + lane_base + kColS + 32u * b, r);
-          tmem_wait_ld();
+        uint32_t r[kTile];
+        if (nrow > 0) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) s[i] = __uint_as_float(r[i]);
+          for (int c = 0; c < kTile / 16; ++c) tmem_ld16(tmem + lane_base + kColS + 64u * b + 16 * c, r + 16 * c);
+          tmem_wait_ld();
         }
         tc_fence_before();
         mbar_arrive(bar(kBarSFree + b));
-        const int pos0 = base + 16 * half;
-        float mx = -CUDART_INF_F;
-        if (lo <= base && hi >= base + kTile) {
+        const uint32_t xbuf = x_slot0 + b * kXBytes;
+        float alpha = 1.f;
+        uint32_t pk[kTile / 2];
+        if (!own) {
+          // Send the partial rows to the owner (its X buffer b must have
+          // been consumed: PV(g-2) is done in both ranks).
+          if (!wwait(bar(kBarPvDone + b), (u & 1u) ^ 1u)) { ok = false; break; }
+          if (valid) {
+            const uint32_t dst = mapa(xbuf, peer);
+            const uint32_t fb = mapa(bar(kBarXFull + 2 * b + slot), peer);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            s[i] *= a.scale_log2;
-            mx = fmaxf(mx, s[i]);
+            for (int j = 0; j < kTile / 4; ++j)
+              st_async_v4(dst + (j * 32 + lane) * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3], fb);
           }
         } else {
+          // Own quarter: add the peer's partial, then the online softmax.
+          if (lane == 0)
+            mbar_arrive_expect_tx(bar(kBarXFull + 2 * b + slot), static_cast<uint32_t>(nrow * kTile * 4));
+          if (!wwait_cluster(bar(kBarXFull + 2 * b + slot), u & 1u)) { ok = false; break; }
+          if (valid) {
+            float s[kTile];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int pos = pos0 + i;
-            s[i] = (pos >= lo && pos < hi) ? s[i] * a.scale_log2 : -CUDART_INF_F;
-            mx = fmaxf(mx, s[i]);
+            for (int j = 0; j < kTile / 4; ++j) {
+              uint32_t x0, x1, x2, x3;
+              ld_shared_v4(xbuf + (j * 32 + lane) * 16, x0, x1, x2, x3);
+              s[4 * j] = __uint_as_float(r[4 * j]) + __uint_as_float(x0);
+              s[4 * j + 1] = __uint_as_float(r[4 * j + 1]) + __uint_as_float(x1);
+              s[4 * j + 2] = __uint_as_float(r[4 * j + 2]) + __uint_as_float(x2);
+              s[4 * j + 3] = __uint_as_float(r[4 * j + 3]) + __uint_as_float(x3);
+            }
+            float mx = -CUDART_INF_F;
+            if (lo <= base && hi >= base + kTile) {
+#pragma unroll
+              for (int i = 0; i < kTile; ++i) {
+                s[i] *= a.scale_log2;
+                mx = fmaxf(mx, s[i]);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < kTile; ++i) {
+                const int pos = base + i;
+                s[i] = (pos >= lo && pos < hi) ? s[i] * a.scale_log2 : -CUDART_INF_F;
+                mx = fmaxf(mx, s[i]);
+              }
+            }
+            if (mx > m + kRescaleThreshold) {
+              alpha = fast_exp2(m - mx);  // 0 on the first tile (m = -inf)
+              l *= alpha;
+              m = mx;
+            }
+            float rs = 0.f;
+#pragma unroll
+            for (int i = 0; i < kTile / 2; ++i) {
+              const float p0 = fast_exp2(s[2 * i] - m), p1 = fast_exp2(s[2 * i + 1] - m);
+              rs += p0 + p1;
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            l += rs;
+          } else {
+#pragma unroll
+            for (int i = 0; i < kTile / 2; ++i) pk[i] = 0;
+          }
+          // P buffer b in TMEM is free once PV(g-2) is done; the peer's single
+          // PX buffer once PV(g-1) is done in both ranks.
+          if (!wwait(bar(kBarPvDone + b), (u & 1u) ^ 1u)) { ok = false; break; }
+          if (g > 0 && !wwait(bar(kBarPvDone + (b ^ 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }
+          if (nrow > 0) tmem_st32(tmem + lane_base + kColP + 32u * b, pk);
+          if (valid) {
+            const uint32_t dst = mapa(px_slot, peer);
+            const uint32_t fb = mapa(bar(kBarPxFull + slot), peer);
+#pragma unroll
+            for (int j = 0; j < kTile / 8; ++j)
+              st_async_v4(dst + (j * 32 + lane) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], fb);
+            st_async_b32(mapa(pxa_slot + lane * 4, peer), __float_as_uint(alpha), fb);
           }
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        float alpha = 1.f;
-        if (mx > m + kRescaleThreshold) {  // same decision in both halves
-          alpha = fast_exp2(m - mx);       // 0 on the first tile (m = -inf)
-          l *= alpha;
-          m = mx;
-        }
-        uint32_t pk[8];
-        float rs = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float p0 = fast_exp2(s[2 * i] - m), p1 = fast_exp2(s[2 * i + 1] - m);
-          rs += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        l += rs;
         // Value rows of this tile outside [lo, hi) may hold anything (stale
         // or unwritten slots): zero this rank's value dims there so that
         // 0 * garbage cannot reach O. QK of the tile is complete here.
         if (lo > base || hi < base + kTile) {
-          const uint32_t v0 = sbase + kOffKV + (g % kStages) * kStageBytes + 4 * rank * kKvChunkBytes;
-          for (int e = tid_sm; e < kTile * 4 * 8; e += 128) {
-            const int r = e >> 5, c = (e >> 3) & 3, piece = e & 7;
-            const int pos = base + r;
-            if (pos < lo || pos >= hi) st_shared_v4(v0 + c * kKvChunkBytes + r * 128 + piece * 16, 0, 0, 0, 0);
+          const uint32_t v0 = sbase + kOffKV + (g % kStages) * kStageBytes;
+          for (int e = tid_sm; e < kTile * kWideChunks * 8; e += 128) {
+            const int rr = e >> 5, c = (e >> 3) & 3, piece = e & 7;
+            const int pos = base + rr;
+            if (pos < lo || pos >= hi) st_shared_v4(v0 + c * kWideBytes + rr * 128 + piece * 16, 0, 0, 0, 0);
           }
+          fence_proxy_async_smem();
         }
-        // (B) P buffer b is free in both ranks once PV(g-2) is done in both.
-        if (!wwait(bar(kBarPvDone + b), (u & 1u) ^ 1u)) { ok = false; break; }
-        if (s_active) {
-          const uint32_t prow = sbase + kOffP + b * kPBytes + gh * 128;
-          const uint32_t prow_peer = mapa(prow, peer);
-          const uint32_t pfull_peer = mapa(bar(kBarPFull + b), peer);
+        if (!own) {
+          // P rows of the owner for this quarter: into this rank's TMEM.
+          if (lane == 0)
+            mbar_arrive_expect_tx(bar(kBarPxFull + slot), static_cast<uint32_t>(nrow * (kTile * 2 + 4)));
+          if (!wwait_cluster(bar(kBarPxFull + slot), g & 1u)) { ok = false; break; }
+          if (nrow > 0) {
+            if (valid) {
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const uint32_t off = ((2 * half + j) ^ (gh & 7)) * 16;
-            st_shared_v4(prow + off, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            st_async_v4(prow_peer + off, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], pfull_peer);
-          }
-          if (half == 0) {
-            const uint32_t aaddr = sbase + kOffAlpha + (b * 128 + gh) * 4;
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(aaddr), "r"(__float_as_uint(alpha)) : "memory");
-            st_async_b32(mapa(aaddr, peer), __float_as_uint(alpha), pfull_peer);
+              for (int j = 0; j < kTile / 8; ++j)
+                ld_shared_v4(px_slot + (j * 32 + lane) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              uint32_t av;
+              asm volatile("ld.shared.b32 %0, [%1];" : "=r"(av) : "r"(pxa_slot + lane * 4) : "memory");
+              alpha = __uint_as_float(av);
+            } else {
+#pragma unroll
+              for (int i = 0; i < kTile / 2; ++i) pk[i] = 0;
+            }
+            tmem_st32(tmem + lane_base + kColP + 32u * b, pk);
           }
         }
-        fence_proxy_async_smem();
-        if (lane == 0)
-          mbar_arrive_expect_tx(bar(kBarPFull + b), static_cast<uint32_t>(peer_rows * kPeerBytesPerRow));
-        else
-          mbar_arrive(bar(kBarPFull + b));
-        // (C) once the peer's rows have landed: rescale, release PV(g).
-        if (!finish_tile(g, blk == w.blk_begin)) { ok = false; break; }
+        // Rescale the O rows of this quarter before PV(g), once PV(g-1) is in.
+        if (!first_tile && nrow > 0 && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
+          if (!wwait(bar(kBarPvDone + (b ^ 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 256 / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld16(tO + c * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(tO + c * 16, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarOFixed + b));
       }
       if (!ok) break;
-      // Epilogue: final row sums of both ranks, wait for the last PV,
-      // normalise, store.
-      l += __shfl_xor_sync(0xffffffffu, l, 16);
-      if (s_active && half == 0) {
-        l_s[gh] = l;
-        st_async_b32(mapa(sbase + kOffL + gh * 4, peer), __float_as_uint(l), mapa(bar(kBarLFull), peer));
-      }
-      if (lane == 0)
-        mbar_arrive_expect_tx(bar(kBarLFull), static_cast<uint32_t>(peer_rows * 4));
-      else
-        mbar_arrive(bar(kBarLFull));
-      if (!wwait_cluster(bar(kBarLFull), n_items & 1u)) { ok = false; break; }
-      if (!wwait(bar(kBarPvDone + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }
-      tc_fence_after();
-      if (s_active && half == 0) {
-        const float lse2 = m + log2f(l);
-        if (w.slot < 0) {
-          if (a.lse) a.lse[static_cast<size_t>(w.b) * H + gh] = lse2 * 0.69314718055994531f;
-        } else {
-          reinterpret_cast<float*>(ws + a.lay.partial_lse)[static_cast<size_t>(w.slot) * H + gh] = lse2;
+      // Epilogue: row sums to the non-owner, wait for the last PV, normalise, store.
+      if (own) {
+        if (valid) st_async_b32(mapa(l_slot + lane * 4, peer), __float_as_uint(l), mapa(bar(kBarLFull + slot), peer));
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarLFull + slot), static_cast<uint32_t>(nrow * 4));
+        if (!wwait_cluster(bar(kBarLFull + slot), n_items & 1u)) { ok = false; break; }
+        if (valid) {
+          uint32_t lv;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(lv) : "r"(l_slot + lane * 4) : "memory");
+          l = __uint_as_float(lv);
         }
       }
-      if (o_warp) {
-        const float inv_l = orow < H ? 1.f / l_s[orow] : 0.f;
+      if (!wwait(bar(kBarPvDone + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }
+      tc_fence_after();
+      if (own && valid) {
+        const float lse2 = m + log2f(l);
+        if (w.slot < 0) {
+          if (a.lse) a.lse[static_cast<size_t>(w.b) * H + row] = lse2 * 0.69314718055994531f;
+        } else {
+          reinterpret_cast<float*>(ws + a.lay.partial_lse)[static_cast<size_t>(w.slot) * H + row] = lse2;
+        }
+      }
+      if (nrow > 0) {
+        const float inv_l = valid ? 1.f / l : 0.f;
 #pragma unroll 1
         for (int c = 0; c < 256 / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld16(tO + c * 32, r);
-          tmem_ld16(tO + c * 32 + 16, r + 16);
+          uint32_t o[32];
+          tmem_ld16(tO + c * 32, o);
+          tmem_ld16(tO + c * 32 + 16, o + 16);
           tmem_wait_ld();
-          if (orow < H) {
+          if (valid) {
             if (w.slot < 0) {
               __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                                   (static_cast<size_t>(w.b) * H + orow) * kDimCkv + dim0 + c * 32;
+                                   (static_cast<size_t>(w.b) * H + row) * kDimCkv + dim0 + c * 32;
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
-                uint4 o;
-                o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
-                o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
-                o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
-                o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
-                reinterpret_cast<uint4*>(dst)[v] = o;
+                uint4 ov;
+                ov.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+                ov.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+                ov.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+                ov.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+                reinterpret_cast<uint4*>(dst)[v] = ov;
               }
             } else {
               float* dst = reinterpret_cast<float*>(ws + a.lay.partial_o) +
-                           (static_cast<size_t>(w.slot) * H + orow) * kDimCkv + dim0 + c * 32;
+                           (static_cast<size_t>(w.slot) * H + row) * kDimCkv + dim0 + c * 32;
 #pragma unroll
               for (int v = 0; v < 8; ++v)
                 reinterpret_cast<float4*>(dst)[v] =
-                    make_float4(__uint_as_float(r[4 * v]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
-                                __uint_as_float(r[4 * v + 2]) * inv_l, __uint_as_float(r[4 * v + 3]) * inv_l);
+                    make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
             }
           }
         }
@@ -602,8 +625,7 @@ int decode_max_active_clusters() {
   return n;
 }
 
-cudaError_t launch_decode(const CUtensorMap& kv_map, const CUtensorMap& q_map, const DecodeArgs& a,
-                          int clusters, cudaStream_t stream) {
+cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& a, int clusters, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -612,8 +634,10 @@ cudaError_t launch_decode(const CUtensorMap& kv_map, const CUtensorMap& q_map, c
     attr_set = true;
   }
   Params p;
-  p.kv_map = kv_map;
-  p.q_map = q_map;
+  p.kv_wide = maps[0];
+  p.kv_narrow = maps[1];
+  p.q_wide = maps[2];
+  p.q_narrow = maps[3];
   p.a = a;
   mla_decode_kernel<<<dim3(2 * clusters), dim3(kThreads), kSmemBytes, stream>>>(p);
   return cudaGetLastError();

@@ -28,9 +28,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D row-major map: rows x cols elements, row pitch `pitch_bytes`, box
-// {box_cols, box_rows}, 128-byte swizzle, zero fill out of bounds.
+// {box_cols, box_rows}, zero fill out of bounds.
 bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t rows, uint64_t cols,
-                 uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows) {
+                 uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -38,7 +39,7 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -117,12 +118,19 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   const int ps = pool->page_size;
   const uint64_t total_rows = static_cast<uint64_t>(pool->num_layers) * pool->num_pages * ps;
   if (total_rows >= (1ull << 31)) return MLA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
-  CUtensorMap kv_map, q_map;
-  if (!make_map_2d(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->data, total_rows, mla::kDimRow,
-                   mla::kDimRow * 2, 64, ps < mla::kBlockTokens ? ps : mla::kBlockTokens))
-    return MLA_ERR_CUDA;
-  if (!make_map_2d(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, static_cast<uint64_t>(batch) * num_heads,
-                   mla::kDimRow, mla::kDimRow * 2, 64, 64))
+  // Each rank of the decode cluster reads 256 c_kv dims as 64-dim boxes
+  // (128-byte swizzle) and 32 rope dims as one 32-dim box (64-byte swizzle).
+  CUtensorMap maps[4];
+  const uint32_t box_rows = ps < mla::kBlockTokens ? ps : mla::kBlockTokens;
+  const uint64_t q_rows = static_cast<uint64_t>(batch) * num_heads;
+  if (!make_map_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->data, total_rows, mla::kDimRow,
+                   mla::kDimRow * 2, 64, box_rows) ||
+      !make_map_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->data, total_rows, mla::kDimRow,
+                   mla::kDimRow * 2, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, q_rows, mla::kDimRow, mla::kDimRow * 2, 64,
+                   128) ||
+      !make_map_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, q_rows, mla::kDimRow, mla::kDimRow * 2, 32,
+                   128, CU_TENSOR_MAP_SWIZZLE_64B))
     return MLA_ERR_CUDA;
 
   mla::DecodeArgs a;
@@ -147,7 +155,7 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   a.kv_scale = pool->kv_scale;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = mla::launch_decode(kv_map, q_map, a, cmax, st);
+  cudaError_t e = mla::launch_decode(maps, a, cmax, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   e = mla::launch_merge(a, st);
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

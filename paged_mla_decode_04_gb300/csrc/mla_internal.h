@@ -14,9 +14,9 @@ constexpr int kDimCkv = 512;
 constexpr int kDimRope = 64;
 constexpr int kDimRow = 576;
 constexpr int kDimV = 128;
-constexpr int kBlockTokens = 32;  // tokens per schedule block = per decode tile
+constexpr int kBlockTokens = 64;  // tokens per schedule block = per decode tile
 
-// One contiguous run of 32-token blocks of one request, processed by one
+// One contiguous run of 64-token blocks of one request, processed by one
 // cluster. Attended positions of the item are [tok_lo, tok_hi).
 struct WorkItem {
   int b;
@@ -110,8 +110,9 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int heads, int p
                         cudaStream_t stream);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream);
 // decode_sm103.cu
-cudaError_t launch_decode(const CUtensorMap& kv_map, const CUtensorMap& q_map, const DecodeArgs& a,
-                          int clusters, cudaStream_t stream);
+// maps: {kv 64-dim boxes (128B swizzle), kv 32-dim boxes (64B swizzle),
+//        q 64-dim boxes, q 32-dim boxes}
+cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& a, int clusters, cudaStream_t stream);
 int decode_max_active_clusters();
 // uv_project.cu
 cudaError_t launch_uv_project(const CUtensorMap& a_map, const CUtensorMap& w_map, void* y,
