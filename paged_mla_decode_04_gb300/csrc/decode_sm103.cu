@@ -55,10 +55,10 @@ constexpr int kXBytes = 2 * 32 * kTile * 4;         // partial S of 2 quarters x
 constexpr int kPxBytes = 2 * 32 * kTile * 2;        // P rows of 2 quarters x 32 rows, bf16
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffX = kOffKV + kStages * kStageBytes;  // [2 buffers]
-constexpr int kOffPx = kOffX + 2 * kXBytes;
-constexpr int kOffPxAlpha = kOffPx + kPxBytes;      // [2 quarters][32] fp32
-constexpr int kOffL = kOffPxAlpha + 256;            // [2 quarters][32] fp32 final row sums
+constexpr int kOffX = kOffKV + kStages * kStageBytes;  // one buffer
+constexpr int kOffPx = kOffX + kXBytes;                // [2 buffers]
+constexpr int kOffPxAlpha = kOffPx + 2 * kPxBytes;  // [2 buffers][2 quarters][32] fp32
+constexpr int kOffL = kOffPxAlpha + 512;            // [2 quarters][32] fp32 final row sums
 constexpr int kOffBar = kOffL + 256;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;    // barriers + alignment slack
 constexpr int kThreads = 224;
@@ -78,9 +78,10 @@ enum Bar {
   kBarQFree,
   kBarSFull,                       // [2]
   kBarSFree = kBarSFull + 2,       // [2]
-  kBarXFull = kBarSFree + 2,       // [2 buffers][2 quarter slots]: peer partial rows landed
-  kBarPxFull = kBarXFull + 4,      // [2 quarter slots]: peer P rows landed
-  kBarOFixed = kBarPxFull + 2,     // [2] P in TMEM and O rescaled for this tile
+  kBarXFull = kBarSFree + 2,       // [2 quarter slots]: peer partial rows landed
+  kBarXFree = kBarXFull + 2,       // [2 quarter slots]: the peer consumed this rank's partial rows
+  kBarPxFull = kBarXFree + 2,      // [2 buffers][2 quarter slots]: peer P rows landed
+  kBarOFixed = kBarPxFull + 4,     // [2] P in TMEM and O rescaled for this tile
   kBarPvDone = kBarOFixed + 2,     // [2] PV on that buffer done in both ranks
   kBarLFull = kBarPvDone + 2,      // [2 quarter slots] final row sums landed
   kBarDrain = kBarLFull + 2,
@@ -155,9 +156,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarSFree + i), 128);
-      mbar_init(bar(kBarXFull + 2 * i), 1);
-      mbar_init(bar(kBarXFull + 2 * i + 1), 1);
-      mbar_init(bar(kBarPxFull + i), 1);
+      mbar_init(bar(kBarXFull + i), 1);
+      mbar_init(bar(kBarXFree + i), 1);
+      mbar_init(bar(kBarPxFull + 2 * i), 1);
+      mbar_init(bar(kBarPxFull + 2 * i + 1), 1);
       mbar_init(bar(kBarOFixed + i), 128);
       mbar_init(bar(kBarPvDone + i), 2);
       mbar_init(bar(kBarLFull + i), 1);
@@ -351,9 +353,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax, exchange, correction, epilogue
     // This warp works on TMEM lane quarter q4: rows (heads) 32 q4 + lane.
-    // The quarter's softmax belongs to rank q4 & 1 ("own" warp here if that
-    // is this rank); the other rank only holds its partial scores and its
-    // share of O. slot = q4 >> 1 indexes the exchange buffers.
+    // The quarter's softmax belongs to rank q4 & 1 ("owner" warp here if
+    // that is this rank); in the other rank the warp only ships its partial
+    // scores to the owner and stores the owner's P rows. slot = q4 >> 1
+    // indexes the exchange buffers.
+    //   owner, tile g:  S(g) + peer partial -> softmax -> P(g) into TMEM and
+    //                   to the peer -> rescale O rows -> release PV(g)
+    //   other, tile g:  S(g) -> partial rows to the owner; then finish tile
+    //                   g-1: its P rows into TMEM -> rescale -> release PV(g-1)
+    // Running the non-owner one tile behind keeps two tiles in the exchange.
     const int q4 = warp & 3;
     const int slot = q4 >> 1;
     const bool own = static_cast<uint32_t>(q4 & 1) == rank;
@@ -363,182 +371,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
     const uint32_t tO = tmem + lane_base + kColO;
     const uint32_t dim0 = 256u * rank;
-    const int tid_sm = threadIdx.x - 64;
     auto wwait = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(b, parity, abort_flag));
     };
     auto wwait_cluster = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait<true>(b, parity, abort_flag));
     };
-    // Exchange buffers: X[b][slot] holds 32 rows x 64 fp32 as 16 groups of
-    // 4 columns, group-major (lane-contiguous 16-byte pieces); PX[slot] holds
-    // 32 rows x 32 packed bf16 pairs, same arrangement.
-    const uint32_t x_slot0 = sbase + kOffX + slot * (32 * kTile * 4);
-    const uint32_t px_slot = sbase + kOffPx + slot * (32 * kTile * 2);
-    const uint32_t pxa_slot = sbase + kOffPxAlpha + slot * 128;
+    // Exchange buffers hold 32 rows as 16-byte pieces, piece-major
+    // (lane-contiguous): X[slot] 64 fp32 per row, PX[b][slot] 32 packed bf16
+    // pairs per row, PXA[b][slot] one rescale factor per row.
+    const uint32_t xbuf = sbase + kOffX + slot * (32 * kTile * 4);
+    auto pxbuf = [&](uint32_t b) { return sbase + kOffPx + b * kPxBytes + slot * (32 * kTile * 2); };
+    auto pxabuf = [&](uint32_t b) { return sbase + kOffPxAlpha + b * 256 + slot * 128; };
     const uint32_t l_slot = sbase + kOffL + slot * 128;
-    uint32_t g = 0, n_items = 0;
-    bool ok = true;
-    for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
-      const WorkItem w = items[it];
-      const int lo = max(w.blk_begin * kTile, w.tok_lo);
-      const int hi = min(w.blk_end * kTile, w.tok_hi);
-      float m = -CUDART_INF_F, l = 0.f;
-      for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++g) {
-        const int base = blk * kTile;
-        const uint32_t b = g & 1u, u = g >> 1;
-        const bool first_tile = blk == w.blk_begin;
-        // Partial scores of this rank for this quarter's rows.
-        if (!wwait(bar(kBarSFull + b), u & 1u)) { ok = false; break; }
+    // Scores of this quarter for tile g (32 x 64 fp32) into r.
+    auto load_scores = [&](uint32_t g, uint32_t* r) -> bool {
+      const uint32_t b = g & 1u, u = g >> 1;
+      if (!wwait(bar(kBarSFull + b), u & 1u)) return false;
+      tc_fence_after();
+      if (nrow > 0) {
+#pragma unroll
+        for (int c = 0; c < kTile / 16; ++c) tmem_ld16(tmem + lane_base + kColS + 64u * b + 16 * c, r + 16 * c);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kBarSFree + b));
+      return true;
+    };
+    // Rescale this quarter's O rows by alpha before PV(g), then release PV(g).
+    auto fix_and_release = [&](uint32_t g, bool first_of_item, float alpha) -> bool {
+      const uint32_t b = g & 1u;
+      if (!first_of_item && nrow > 0 && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
+        if (!wwait(bar(kBarPvDone + (b ^ 1u)), ((g - 1) >> 1) & 1u)) return false;  // PV(g-1) is in O
         tc_fence_after();
-        uint32_t r[kTile];
-        if (nrow > 0) {
-#pragma unroll
-          for (int c = 0; c < kTile / 16; ++c) tmem_ld16(tmem + lane_base + kColS + 64u * b + 16 * c, r + 16 * c);
-          tmem_wait_ld();
-        }
-        tc_fence_before();
-        mbar_arrive(bar(kBarSFree + b));
-        const uint32_t xbuf = x_slot0 + b * kXBytes;
-        float alpha = 1.f;
-        uint32_t pk[kTile / 2];
-        if (!own) {
-          // Send the partial rows to the owner (its X buffer b must have
-          // been consumed: PV(g-2) is done in both ranks).
-          if (!wwait(bar(kBarPvDone + b), (u & 1u) ^ 1u)) { ok = false; break; }
-          if (valid) {
-            const uint32_t dst = mapa(xbuf, peer);
-            const uint32_t fb = mapa(bar(kBarXFull + 2 * b + slot), peer);
-#pragma unroll
-            for (int j = 0; j < kTile / 4; ++j)
-              st_async_v4(dst + (j * 32 + lane) * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3], fb);
-          }
-        } else {
-          // Own quarter: add the peer's partial, then the online softmax.
-          if (lane == 0)
-            mbar_arrive_expect_tx(bar(kBarXFull + 2 * b + slot), static_cast<uint32_t>(nrow * kTile * 4));
-          if (!wwait_cluster(bar(kBarXFull + 2 * b + slot), u & 1u)) { ok = false; break; }
-          if (valid) {
-            float s[kTile];
-#pragma unroll
-            for (int j = 0; j < kTile / 4; ++j) {
-              uint32_t x0, x1, x2, x3;
-              ld_shared_v4(xbuf + (j * 32 + lane) * 16, x0, x1, x2, x3);
-              s[4 * j] = __uint_as_float(r[4 * j]) + __uint_as_float(x0);
-              s[4 * j + 1] = __uint_as_float(r[4 * j + 1]) + __uint_as_float(x1);
-              s[4 * j + 2] = __uint_as_float(r[4 * j + 2]) + __uint_as_float(x2);
-              s[4 * j + 3] = __uint_as_float(r[4 * j + 3]) + __uint_as_float(x3);
-            }
-            float mx = -CUDART_INF_F;
-            if (lo <= base && hi >= base + kTile) {
-#pragma unroll
-              for (int i = 0; i < kTile; ++i) {
-                s[i] *= a.scale_log2;
-                mx = fmaxf(mx, s[i]);
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < kTile; ++i) {
-                const int pos = base + i;
-                s[i] = (pos >= lo && pos < hi) ? s[i] * a.scale_log2 : -CUDART_INF_F;
-                mx = fmaxf(mx, s[i]);
-              }
-            }
-            if (mx > m + kRescaleThreshold) {
-              alpha = fast_exp2(m - mx);  // 0 on the first tile (m = -inf)
-              l *= alpha;
-              m = mx;
-            }
-            float rs = 0.f;
-#pragma unroll
-            for (int i = 0; i < kTile / 2; ++i) {
-              const float p0 = fast_exp2(s[2 * i] - m), p1 = fast_exp2(s[2 * i + 1] - m);
-              rs += p0 + p1;
-              pk[i] = pack_bf16x2(p0, p1);
-            }
-            l += rs;
-          } else {
-#pragma unroll
-            for (int i = 0; i < kTile / 2; ++i) pk[i] = 0;
-          }
-          // P buffer b in TMEM is free once PV(g-2) is done; the peer's single
-          // PX buffer once PV(g-1) is done in both ranks.
-          if (!wwait(bar(kBarPvDone + b), (u & 1u) ^ 1u)) { ok = false; break; }
-          if (g > 0 && !wwait(bar(kBarPvDone + (b ^ 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }
-          if (nrow > 0) tmem_st32(tmem + lane_base + kColP + 32u * b, pk);
-          if (valid) {
-            const uint32_t dst = mapa(px_slot, peer);
-            const uint32_t fb = mapa(bar(kBarPxFull + slot), peer);
-#pragma unroll
-            for (int j = 0; j < kTile / 8; ++j)
-              st_async_v4(dst + (j * 32 + lane) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], fb);
-            st_async_b32(mapa(pxa_slot + lane * 4, peer), __float_as_uint(alpha), fb);
-          }
-        }
-        // Value rows of this tile outside [lo, hi) may hold anything (stale
-        // or unwritten slots): zero this rank's value dims there so that
-        // 0 * garbage cannot reach O. QK of the tile is complete here.
-        if (lo > base || hi < base + kTile) {
-          const uint32_t v0 = sbase + kOffKV + (g % kStages) * kStageBytes;
-          for (int e = tid_sm; e < kTile * kWideChunks * 8; e += 128) {
-            const int rr = e >> 5, c = (e >> 3) & 3, piece = e & 7;
-            const int pos = base + rr;
-            if (pos < lo || pos >= hi) st_shared_v4(v0 + c * kWideBytes + rr * 128 + piece * 16, 0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-        }
-        if (!own) {
-          // P rows of the owner for this quarter: into this rank's TMEM.
-          if (lane == 0)
-            mbar_arrive_expect_tx(bar(kBarPxFull + slot), static_cast<uint32_t>(nrow * (kTile * 2 + 4)));
-          if (!wwait_cluster(bar(kBarPxFull + slot), g & 1u)) { ok = false; break; }
-          if (nrow > 0) {
-            if (valid) {
-#pragma unroll
-              for (int j = 0; j < kTile / 8; ++j)
-                ld_shared_v4(px_slot + (j * 32 + lane) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-              uint32_t av;
-              asm volatile("ld.shared.b32 %0, [%1];" : "=r"(av) : "r"(pxa_slot + lane * 4) : "memory");
-              alpha = __uint_as_float(av);
-            } else {
-#pragma unroll
-              for (int i = 0; i < kTile / 2; ++i) pk[i] = 0;
-            }
-            tmem_st32(tmem + lane_base + kColP + 32u * b, pk);
-          }
-        }
-        // Rescale the O rows of this quarter before PV(g), once PV(g-1) is in.
-        if (!first_tile && nrow > 0 && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
-          if (!wwait(bar(kBarPvDone + (b ^ 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }
-          tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 256 / 16; ++c) {
-            uint32_t o[16];
-            tmem_ld16(tO + c * 16, o);
-            tmem_wait_ld();
+        for (int c = 0; c < 256 / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld16(tO + c * 16, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st16(tO + c * 16, o);
-          }
+          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st16(tO + c * 16, o);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(kBarOFixed + b));
       }
-      if (!ok) break;
-      // Epilogue: row sums to the non-owner, wait for the last PV, normalise, store.
-      if (own) {
-        if (valid) st_async_b32(mapa(l_slot + lane * 4, peer), __float_as_uint(l), mapa(bar(kBarLFull + slot), peer));
-      } else {
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarLFull + slot), static_cast<uint32_t>(nrow * 4));
-        if (!wwait_cluster(bar(kBarLFull + slot), n_items & 1u)) { ok = false; break; }
+      tmem_wait_st();
+      tc_fence_before();
+      // Arrive for tile g only after tile g-2 (same buffer) has been
+      // released by every warp: a warp with no heads in its quarter waits on
+      // nothing else and could otherwise arrive twice in one phase.
+      if (!wwait(bar(kBarPvDone + b), ((g >> 1) & 1u) ^ 1u)) return false;
+      mbar_arrive(bar(kBarOFixed + b));
+      return true;
+    };
+    // Non-owner: the owner's P rows of tile g into TMEM, then release.
+    auto finish_tile = [&](uint32_t g, bool first_of_item) -> bool {
+      const uint32_t b = g & 1u, u = g >> 1;
+      float alpha = 1.f;
+      if (nrow > 0) {
+        if (lane == 0)
+          mbar_arrive_expect_tx(bar(kBarPxFull + 2 * b + slot), static_cast<uint32_t>(nrow * (kTile * 2 + 4)));
+        if (!wwait_cluster(bar(kBarPxFull + 2 * b + slot), u & 1u)) return false;
+        uint32_t pk[kTile / 2];
         if (valid) {
-          uint32_t lv;
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(lv) : "r"(l_slot + lane * 4) : "memory");
-          l = __uint_as_float(lv);
+#pragma unroll
+          for (int j = 0; j < kTile / 8; ++j)
+            ld_shared_v4(pxbuf(b) + (j * 32 + lane) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          uint32_t av;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(av) : "r"(pxabuf(b) + lane * 4) : "memory");
+          alpha = __uint_as_float(av);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kTile / 2; ++i) pk[i] = 0;
         }
+        tmem_st32(tmem + lane_base + kColP + 32u * b, pk);
       }
-      if (!wwait(bar(kBarPvDone + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }
+      return fix_and_release(g, first_of_item, alpha);
+    };
+    // Epilogue of an item: wait for its last PV, normalise, store.
+    auto store_item = [&](const WorkItem& w, uint32_t g_last, float m, float l) -> bool {
+      if (!wwait(bar(kBarPvDone + (g_last & 1u)), (g_last >> 1) & 1u)) return false;
       tc_fence_after();
       if (own && valid) {
         const float lse2 = m + log2f(l);
@@ -582,6 +493,133 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
+      return true;
+    };
+    uint32_t g = 0, n_items = 0;
+    bool ok = true;
+    for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
+      const WorkItem w = items[it];
+      const int lo = max(w.blk_begin * kTile, w.tok_lo);
+      const int hi = min(w.blk_end * kTile, w.tok_hi);
+      float m = -CUDART_INF_F, l = 0.f;
+      for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++g) {
+        const int base = blk * kTile;
+        const uint32_t b = g & 1u, u = g >> 1;
+        const bool first_tile = blk == w.blk_begin;
+        uint32_t r[kTile];
+        if (!load_scores(g, r)) { ok = false; break; }
+        if (!own) {
+          // Ship the partial rows once the owner has consumed the previous
+          // ones. Quarters without heads exchange nothing and skip the
+          // handshake (an idle owner would otherwise run phases ahead).
+          if (nrow > 0 && !wwait(bar(kBarXFree + slot), (g & 1u) ^ 1u)) { ok = false; break; }
+          if (valid) {
+            const uint32_t dst = mapa(xbuf, peer);
+            const uint32_t fb = mapa(bar(kBarXFull + slot), peer);
+#pragma unroll
+            for (int j = 0; j < kTile / 4; ++j)
+              st_async_v4(dst + (j * 32 + lane) * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3], fb);
+          }
+          if (!first_tile && !finish_tile(g - 1, blk - 1 == w.blk_begin)) { ok = false; break; }
+          continue;
+        }
+        // Owner: add the peer's partial, then the online softmax.
+        if (nrow > 0) {
+          if (lane == 0) mbar_arrive_expect_tx(bar(kBarXFull + slot), static_cast<uint32_t>(nrow * kTile * 4));
+          if (!wwait_cluster(bar(kBarXFull + slot), g & 1u)) { ok = false; break; }
+        }
+        float alpha = 1.f;
+        uint32_t pk[kTile / 2];
+        float s[kTile];
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < kTile / 4; ++j) {
+            uint32_t x0, x1, x2, x3;
+            ld_shared_v4(xbuf + (j * 32 + lane) * 16, x0, x1, x2, x3);
+            s[4 * j] = __uint_as_float(r[4 * j]) + __uint_as_float(x0);
+            s[4 * j + 1] = __uint_as_float(r[4 * j + 1]) + __uint_as_float(x1);
+            s[4 * j + 2] = __uint_as_float(r[4 * j + 2]) + __uint_as_float(x2);
+            s[4 * j + 3] = __uint_as_float(r[4 * j + 3]) + __uint_as_float(x3);
+          }
+        }
+        __syncwarp();
+        if (nrow > 0 && lane == 0) mbar_arrive_remote_relaxed(mapa(bar(kBarXFree + slot), peer));  // X consumed
+        if (valid) {
+          float mx = -CUDART_INF_F;
+          if (lo <= base && hi >= base + kTile) {
+#pragma unroll
+            for (int i = 0; i < kTile; ++i) {
+              s[i] *= a.scale_log2;
+              mx = fmaxf(mx, s[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < kTile; ++i) {
+              const int pos = base + i;
+              s[i] = (pos >= lo && pos < hi) ? s[i] * a.scale_log2 : -CUDART_INF_F;
+              mx = fmaxf(mx, s[i]);
+            }
+          }
+          if (mx > m + kRescaleThreshold) {
+            alpha = fast_exp2(m - mx);  // 0 on the first tile (m = -inf)
+            l *= alpha;
+            m = mx;
+          }
+          float rs = 0.f;
+#pragma unroll
+          for (int i = 0; i < kTile / 2; ++i) {
+            const float p0 = fast_exp2(s[2 * i] - m), p1 = fast_exp2(s[2 * i + 1] - m);
+            rs += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          l += rs;
+        } else {
+#pragma unroll
+          for (int i = 0; i < kTile / 2; ++i) pk[i] = 0;
+        }
+        // Value rows of this tile outside [lo, hi) may hold anything (stale
+        // or unwritten slots): zero this rank's value dims there so that
+        // 0 * garbage cannot reach O. QK of the tile is complete here.
+        if (lo > base || hi < base + kTile) {
+          const uint32_t v0 = sbase + kOffKV + (g % kStages) * kStageBytes;
+          const int t64 = 32 * slot + lane;  // 0..63 over the two owner warps
+          for (int e = t64; e < kTile * kWideChunks * 8; e += 64) {
+            const int rr = e >> 5, c = (e >> 3) & 3, piece = e & 7;
+            const int pos = base + rr;
+            if (pos < lo || pos >= hi) st_shared_v4(v0 + c * kWideBytes + rr * 128 + piece * 16, 0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        // TMEM P[b] and the peer's PX[b] are free once PV(g-2) is done in both ranks.
+        if (!wwait(bar(kBarPvDone + b), (u & 1u) ^ 1u)) { ok = false; break; }
+        if (nrow > 0) tmem_st32(tmem + lane_base + kColP + 32u * b, pk);
+        if (valid) {
+          const uint32_t dst = mapa(pxbuf(b), peer);
+          const uint32_t fb = mapa(bar(kBarPxFull + 2 * b + slot), peer);
+#pragma unroll
+          for (int j = 0; j < kTile / 8; ++j)
+            st_async_v4(dst + (j * 32 + lane) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], fb);
+          st_async_b32(mapa(pxabuf(b) + lane * 4, peer), __float_as_uint(alpha), fb);
+        }
+        if (!fix_and_release(g, first_tile, alpha)) { ok = false; break; }
+      }
+      if (!ok) break;
+      // Row sums to the non-owner; the non-owner finishes its last tile first.
+      if (own) {
+        if (valid) st_async_b32(mapa(l_slot + lane * 4, peer), __float_as_uint(l), mapa(bar(kBarLFull + slot), peer));
+      } else {
+        if (!finish_tile(g - 1, w.blk_end - 1 == w.blk_begin)) { ok = false; break; }
+        if (nrow > 0) {
+          if (lane == 0) mbar_arrive_expect_tx(bar(kBarLFull + slot), static_cast<uint32_t>(nrow * 4));
+          if (!wwait_cluster(bar(kBarLFull + slot), n_items & 1u)) { ok = false; break; }
+        }
+        if (valid) {
+          uint32_t lv;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(lv) : "r"(l_slot + lane * 4) : "memory");
+          l = __uint_as_float(lv);
+        }
+      }
+      if (!store_item(w, g - 1, m, l)) { ok = false; break; }
     }
     if (!ok) {
       *abort_flag = 1;
