@@ -165,6 +165,37 @@ int mla_uv_project(const void* attn_out, const void* w_uv, void* y, int batch,
  * `clear` is nonzero, resets it. Synchronises `stream`: diagnostics only. */
 int mla_get_error(void* workspace, int* code, int clear, void* stream);
 
+/* Allocation-free decode, for callers that cannot allocate device memory at
+ * all: code running inside a memory pool or arena that it does not own,
+ * plugins whose host forbids cudaMalloc while a graph or a tight memory
+ * budget is active, or embedded runtimes that only hand out fixed buffers.
+ * The paper has no counterpart of this call; it is the same operation as
+ * mla_decode_plan followed by mla_decode (same arguments, same results),
+ * with the schedule and the split partials kept in a scratch array that the
+ * library declares at file scope (MLA_NOALLOC_SCRATCH_BYTES of device
+ * memory, held by every GPU that loads the library until the process ends).
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - A call needs mla_decode_workspace_size(batch, num_heads) bytes of that
+ *     scratch: on a 152-SM GPU about 38 MiB of split partials at 128 heads
+ *     plus 64 bytes per request, so up to about 150,000 requests fit; a
+ *     larger call returns MLA_ERR_WORKSPACE without launching anything.
+ *   - The first call on a device looks up the scratch array's device
+ *     address; make that first call before any stream capture.
+ *   - Every call shares the one scratch array: calls whose work overlaps on
+ *     the GPU (different streams, no ordering between them) race. Order them
+ *     on one stream.
+ *   - The scratch keeps the last call's contents; each call resets its
+ *     status word first. status (device int32 or NULL) receives the
+ *     MLA_STATUS_* bits of this call when the decode has finished.
+ *   - num_clusters as in mla_decode_plan (0 = full width). */
+#define MLA_NOALLOC_SCRATCH_BYTES (48u << 20)
+int mla_decode_noalloc(const mla_kv_pool* pool, int layer, const void* q,
+                       const int32_t* page_indptr, const int32_t* page_ids,
+                       int max_blocks, const int32_t* context_lens, int batch,
+                       int num_heads, float softmax_scale, int window,
+                       int num_clusters, void* out, float* lse,
+                       int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

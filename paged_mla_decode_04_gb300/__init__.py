@@ -39,7 +39,9 @@ KV_LORA_RANK = 512
 V_HEAD_DIM = 128
 
 EXPORTED = ["mla_kv_write", "mla_decode_workspace_size", "mla_decode_num_clusters",
-            "mla_decode_plan", "mla_decode", "mla_uv_project", "mla_get_error"]
+            "mla_decode_plan", "mla_decode", "mla_uv_project", "mla_get_error",
+            "mla_decode_noalloc"]
+NOALLOC_SCRATCH_BYTES = 48 << 20
 
 
 class MlaError(RuntimeError):
@@ -79,6 +81,9 @@ def load_library(path: str = LIB_PATH):
     lib.mla_uv_project.restype = I
     lib.mla_get_error.argtypes = [P, ctypes.POINTER(I), I, P]
     lib.mla_get_error.restype = I
+    lib.mla_decode_noalloc.argtypes = [ctypes.POINTER(_Pool), I, P, P, P, I, P, I, I, ctypes.c_float,
+                                       I, I, P, P, P, P]
+    lib.mla_decode_noalloc.restype = I
     _lib = lib
     return lib
 
@@ -213,6 +218,28 @@ def uv_project(attn_out: torch.Tensor, w_uv: torch.Tensor, y: torch.Tensor, stre
                             _stream(stream))
     _check(rc, "mla_uv_project")
     return y
+
+
+def decode_noalloc(pool: KVPool, layer: int, q: torch.Tensor, context_lens: torch.Tensor,
+                   softmax_scale: float, out: torch.Tensor, block_table: torch.Tensor,
+                   window: int = 0, num_clusters: int = 0, lse: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """mla_decode_plan + mla_decode without a caller workspace: the library's
+    fixed scratch array holds the schedule and partials (see the C header for
+    the size limit and the one-stream rule)."""
+    lib = load_library()
+    B, H, _ = q.shape
+    c = pool._c()
+    rc = lib.mla_decode_noalloc(ctypes.byref(c), layer, _dev(q, "q", torch.bfloat16), None,
+                                _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+                                _dev(context_lens, "context_lens", torch.int32), B, H,
+                                float(softmax_scale), window, num_clusters,
+                                _dev(out, "out", torch.bfloat16),
+                                None if lse is None else _dev(lse, "lse", torch.float32),
+                                None if status is None else _dev(status, "status", torch.int32),
+                                _stream(stream))
+    _check(rc, "mla_decode_noalloc")
+    return out
 
 
 def get_error(workspace: torch.Tensor, clear: bool = False, stream=None) -> int:

@@ -9,6 +9,9 @@
 #include "../../include/mla_decode.h"
 #include "mla_internal.h"
 
+// Scratch of mla_decode_noalloc: schedule, status and split partials.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 using mla::WsHeader;
@@ -55,6 +58,21 @@ bool valid_pool(const mla_kv_pool* pool) {
 }
 
 int max_clusters() { return mla::decode_max_active_clusters(); }
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the host-side symbol is only a stand-in for it).
+void* noalloc_scratch() {
+  constexpr int kMaxDevices = 64;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
 
 }  // namespace
 
@@ -185,6 +203,32 @@ int mla_uv_project(const void* attn_out, const void* w_uv, void* y, int batch, i
     return MLA_ERR_CUDA;
   cudaError_t e = mla::launch_uv_project(a_map, w_map, y, batch, num_heads, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_decode_noalloc(const mla_kv_pool* pool, int layer, const void* q, const int32_t* page_indptr,
+                       const int32_t* page_ids, int max_blocks, const int32_t* context_lens, int batch,
+                       int num_heads, float softmax_scale, int window, int num_clusters, void* out, float* lse,
+                       int32_t* status, void* stream) {
+  if (!valid_pool(pool) || batch < 0 || window < 0 || num_clusters < 0) return MLA_ERR_ARG;
+  if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
+  const int cmax = max_clusters();
+  if (cmax <= 0) return MLA_ERR_CUDA;
+  const size_t need = mla::ws_layout(batch, num_heads, cmax).total;
+  if (need > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
+  void* ws = noalloc_scratch();
+  if (!ws) return MLA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The scratch keeps the previous call's bytes: start this call's status at 0.
+  if (cudaMemsetAsync(ws, 0, sizeof(mla::WsHeader), st) != cudaSuccess) return MLA_ERR_CUDA;
+  int rc = mla_decode_plan(context_lens, batch, num_heads, pool->page_size, window, num_clusters, ws, need,
+                           stream);
+  if (rc != MLA_OK) return rc;
+  rc = mla_decode(pool, layer, q, page_indptr, page_ids, max_blocks, context_lens, batch, num_heads,
+                  softmax_scale, window, ws, out, lse, stream);
+  if (rc != MLA_OK) return rc;
+  if (status && cudaMemcpyAsync(status, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 int mla_get_error(void* workspace, int* code, int clear, void* stream) {

@@ -1,0 +1,57 @@
+"""The allocation-free decode entry point (mla_decode_noalloc), called
+through the C ABI, against the workspace entry points (mla_decode_plan +
+mla_decode) on the same inputs: same results within the parity tolerance,
+on two calls in a row (the shared scratch keeps the previous call's bytes).
+This file sorts last so that a run stopping at the first failure has run
+every other test before it."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import mla_workloads as mw
+from mla_testlib import TOL_BF16, DeviceWorkload, f64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name,heads,lens", [("v3", 128, [3000, 17, 900, 2500, 0, 64]),
+                                             ("v2lite", 16, [2992, 130, 1333, 3992])])
+def test_noalloc_decode_matches_workspace_decode_twice(name, heads, lens):
+    import paged_mla_decode_04_gb300 as m
+    lib = m.load_library()
+    wl = mw.make(name, num_heads=heads, context_lens=lens)
+    dw = DeviceWorkload(wl, m)
+    ref_out, ref_lse = dw.step()          # writes the new rows, then plan + decode
+    stream = torch.cuda.current_stream().cuda_stream
+    pool = dw.pool._c()
+    for call in range(2):
+        out = torch.full_like(dw.out, float("nan"))
+        lse = torch.full_like(dw.lse, float("nan"))
+        status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        rc = lib.mla_decode_noalloc(ctypes.byref(pool), wl.layer, dw.q.data_ptr(), None,
+                                    dw.block_table.data_ptr(), dw.block_table.shape[1],
+                                    dw.lens.data_ptr(), wl.batch, wl.num_heads,
+                                    ctypes.c_float(wl.softmax_scale), wl.window, 0,
+                                    out.data_ptr(), lse.data_ptr(), status.data_ptr(), stream)
+        assert rc == 0, "call %d returned %d" % (call, rc)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        got = f64(out)
+        assert rel_err(got, ref_out) <= TOL_BF16, "call %d" % call
+        assert np.abs(lse.cpu().numpy() - ref_lse).max() <= 1e-3 * max(1.0, np.abs(ref_lse).max())
+
+
+def test_noalloc_rejects_calls_beyond_its_scratch():
+    import paged_mla_decode_04_gb300 as m
+    lib = m.load_library()
+    wl = mw.make("tiny")
+    dw = DeviceWorkload(wl, m)
+    pool = dw.pool._c()
+    too_many = 1 << 20                    # far beyond what the fixed scratch holds
+    rc = lib.mla_decode_noalloc(ctypes.byref(pool), 0, dw.q.data_ptr(), None,
+                                dw.block_table.data_ptr(), dw.block_table.shape[1],
+                                dw.lens.data_ptr(), too_many, 128, ctypes.c_float(0.07), 0, 0,
+                                dw.out.data_ptr(), None, None, 0)
+    assert rc == -3                       # MLA_ERR_WORKSPACE, nothing launched
