@@ -18,20 +18,21 @@
 //     (288 dims) and of q; it gathers its slice of each 64-token tile by TMA
 //     (one box per page and chunk, 3-stage ring) and computes a partial
 //     S_r = Q_r K_r^T for all heads with tcgen05.mma M=128 x N=64 into TMEM;
-//   - the heads are split by TMEM lane quarter: quarter q belongs to rank
-//     q & 1. Each rank sends the partial rows of the other rank's heads with
-//     st.async (fp32, 16 KB per tile), adds the peer's partial to its own
-//     heads, runs their online softmax (base 2, lazy rescale: the reference
-//     max moves only when the running max grows by more than 8, the final
-//     1/l makes the result exact), keeps its P rows in TMEM and sends them
-//     (bf16, with the rescale factor) to the peer, which stores them in its
-//     TMEM too;
+//   - each rank rounds its partial scores to bf16 and sends them to the
+//     peer (st.async, 16 KB per tile), so both ranks form the same sum
+//     bf16(S_0) + bf16(S_1) (fp32 addition commutes) and run the same online
+//     softmax for all heads (base 2, lazy rescale: the reference max moves
+//     only when the running max grows by more than 8, the final 1/l makes
+//     the result exact), each keeping P in its own TMEM. One exchange per
+//     tile and no P traffic: SM-to-SM bandwidth and latency, not the tensor
+//     pipe, bound this design. The rounding puts a relative error of at most
+//     2^-8 of the larger half's partial score on each score;
 //   - each rank accumulates O for all heads over its 256 value dims with
 //     tcgen05.mma M=128 x N=256 x K=64, P read from TMEM and V read MN-major
 //     straight from the gathered tile.
 // Warp roles per CTA (224 threads): warp 0 TMA producer, warp 1 TMEM owner
-// and QK issuer, warps 2-5 softmax / exchange / correction / epilogue (warp
-// w works on TMEM lane quarter w & 3), warp 6 PV issuer.
+// and QK issuer, warps 2-5 exchange / softmax / correction / epilogue (warp
+// w works on TMEM lane quarter w & 3, one head per thread), warp 6 PV issuer.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -51,16 +52,12 @@ constexpr int kStageBytes = kWideChunks * kWideBytes + kNarrowBytes;   // 36 KB
 constexpr int kQWideBytes = 128 * 128;              // [128 heads][64 dims]
 constexpr int kQNarrowBytes = 128 * 64;             // [128 heads][32 rope dims]
 constexpr int kQBytes = kWideChunks * kQWideBytes + kQNarrowBytes;     // 72 KB
-constexpr int kXBytes = 2 * 32 * kTile * 4;         // partial S of 2 quarters x 32 rows, fp32
-constexpr int kPxBytes = 2 * 32 * kTile * 2;        // P rows of 2 quarters x 32 rows, bf16
+constexpr int kXBytes = 128 * kTile * 2;            // the peer's partial S of 128 rows, bf16
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffX = kOffKV + kStages * kStageBytes;  // one buffer
-constexpr int kOffPx = kOffX + kXBytes;                // [2 buffers]
-constexpr int kOffPxAlpha = kOffPx + 2 * kPxBytes;  // [2 buffers][2 quarters][32] fp32
-constexpr int kOffL = kOffPxAlpha + 512;            // [2 quarters][32] fp32 final row sums
-constexpr int kOffBar = kOffL + 256;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;    // barriers + alignment slack
+constexpr int kOffX = kOffKV + kStages * kStageBytes;  // [2 buffers]
+constexpr int kOffBar = kOffX + 2 * kXBytes;
+constexpr int kSmemBytes = kOffBar + 512 + 1024;    // barriers + alignment slack
 constexpr int kThreads = 224;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                       // O: [0, 256)
@@ -78,17 +75,15 @@ enum Bar {
   kBarQFree,
   kBarSFull,                       // [2]
   kBarSFree = kBarSFull + 2,       // [2]
-  kBarXFull = kBarSFree + 2,       // [2 quarter slots]: peer partial rows landed
-  kBarXFree = kBarXFull + 2,       // [2 quarter slots]: the peer consumed this rank's partial rows
-  kBarPxFull = kBarXFree + 2,      // [2 buffers][2 quarter slots]: peer P rows landed
-  kBarOFixed = kBarPxFull + 4,     // [2] P in TMEM and O rescaled for this tile
-  kBarPvDone = kBarOFixed + 2,     // [2] PV on that buffer done in both ranks
-  kBarLFull = kBarPvDone + 2,      // [2 quarter slots] final row sums landed
-  kBarDrain = kBarLFull + 2,
+  kBarXFull = kBarSFree + 2,       // [2 buffers][4 quarters]: the peer's partial rows landed
+  kBarXFree = kBarXFull + 8,       // [2 buffers][4 quarters]: the peer read this rank's partial rows
+  kBarOFixed = kBarXFree + 8,      // [2] P in TMEM and O rescaled for this tile
+  kBarPvDone = kBarOFixed + 2,     // [2] PV on that buffer done
+  kBarDrain = kBarPvDone + 2,
   kBarDrainPv,
   kNumBars
 };
-static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+static_assert(kNumBars * 8 + 8 <= 512, "barrier area");
 
 struct Params {
   CUtensorMap kv_wide;    // pool rows [NL*P*ps][576] bf16, box {64, rows}, 128B swizzle
@@ -156,13 +151,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarSFree + i), 128);
+      mbar_init(bar(kBarOFixed + i), 128);
+      mbar_init(bar(kBarPvDone + i), 1);
+    }
+    for (int i = 0; i < 8; ++i) {
       mbar_init(bar(kBarXFull + i), 1);
       mbar_init(bar(kBarXFree + i), 1);
-      mbar_init(bar(kBarPxFull + 2 * i), 1);
-      mbar_init(bar(kBarPxFull + 2 * i + 1), 1);
-      mbar_init(bar(kBarOFixed + i), 128);
-      mbar_init(bar(kBarPvDone + i), 2);
-      mbar_init(bar(kBarLFull + i), 1);
     }
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarDrainPv), 1);
@@ -340,7 +334,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mma_bf16_ts(tO, tmem + kColP + 32u * b + 8u * k, sdesc_sw128(v0 + k * 16 * 128, kWideBytes, 1024),
                         idesc_pv, (t | k) != 0);
           mma_commit(bar(kBarKvEmpty + g % kStages));
-          mma_commit_both(bar(kBarPvDone + b));
+          mma_commit(bar(kBarPvDone + b));
         }
       }
       if (!ok) {
@@ -351,20 +345,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_wait(bar(kBarDrainPv), 0, nullptr);
     }
   } else {
-    // ------------------------------------------------------------ softmax, exchange, correction, epilogue
-    // This warp works on TMEM lane quarter q4: rows (heads) 32 q4 + lane.
-    // The quarter's softmax belongs to rank q4 & 1 ("owner" warp here if
-    // that is this rank); in the other rank the warp only ships its partial
-    // scores to the owner and stores the owner's P rows. slot = q4 >> 1
-    // indexes the exchange buffers.
-    //   owner, tile g:  S(g) + peer partial -> softmax -> P(g) into TMEM and
-    //                   to the peer -> rescale O rows -> release PV(g)
-    //   other, tile g:  S(g) -> partial rows to the owner; then finish tile
-    //                   g-1: its P rows into TMEM -> rescale -> release PV(g-1)
-    // Running the non-owner one tile behind keeps two tiles in the exchange.
+    // ------------------------------------------------------------ exchange, softmax, correction, epilogue
+    // Warp w works on TMEM lane quarter q4 = w & 3: rows (heads) 32 q4 + lane,
+    // one head per thread. Per tile g: this rank's partial scores of the
+    // quarter, rounded to bf16, go to the peer (st.async, 4 KB) and the
+    // peer's arrive the same way; both ranks then form the same sum
+    // bf16(S_0) + bf16(S_1) (fp32 addition commutes), so both run the same
+    // online softmax (base 2, lazy rescale: the reference max moves only
+    // when the running max grows by more than 8; the final 1/l keeps the
+    // result exact) and keep the same P in their own TMEM. One exchange per
+    // tile, no P traffic, and every SM sub-partition takes a quarter of the
+    // exponentials.
     const int q4 = warp & 3;
-    const int slot = q4 >> 1;
-    const bool own = static_cast<uint32_t>(q4 & 1) == rank;
     const int nrow = min(max(H - 32 * q4, 0), 32);  // valid heads in this quarter
     const int row = 32 * q4 + lane;                 // head of this lane
     const bool valid = lane < nrow;
@@ -377,81 +369,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto wwait_cluster = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait<true>(b, parity, abort_flag));
     };
-    // Exchange buffers hold 32 rows as 16-byte pieces, piece-major
-    // (lane-contiguous): X[slot] 64 fp32 per row, PX[b][slot] 32 packed bf16
-    // pairs per row, PXA[b][slot] one rescale factor per row.
-    const uint32_t xbuf = sbase + kOffX + slot * (32 * kTile * 4);
-    auto pxbuf = [&](uint32_t b) { return sbase + kOffPx + b * kPxBytes + slot * (32 * kTile * 2); };
-    auto pxabuf = [&](uint32_t b) { return sbase + kOffPxAlpha + b * 256 + slot * 128; };
-    const uint32_t l_slot = sbase + kOffL + slot * 128;
-    // Scores of this quarter for tile g (32 x 64 fp32) into r.
-    auto load_scores = [&](uint32_t g, uint32_t* r) -> bool {
-      const uint32_t b = g & 1u, u = g >> 1;
-      if (!wwait(bar(kBarSFull + b), u & 1u)) return false;
-      tc_fence_after();
-      if (nrow > 0) {
-#pragma unroll
-        for (int c = 0; c < kTile / 16; ++c) tmem_ld16(tmem + lane_base + kColS + 64u * b + 16 * c, r + 16 * c);
-        tmem_wait_ld();
-      }
-      tc_fence_before();
-      mbar_arrive(bar(kBarSFree + b));
-      return true;
-    };
-    // Rescale this quarter's O rows by alpha before PV(g), then release PV(g).
-    auto fix_and_release = [&](uint32_t g, bool first_of_item, float alpha) -> bool {
-      const uint32_t b = g & 1u;
-      if (!first_of_item && nrow > 0 && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
-        if (!wwait(bar(kBarPvDone + (b ^ 1u)), ((g - 1) >> 1) & 1u)) return false;  // PV(g-1) is in O
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 256 / 16; ++c) {
-          uint32_t o[16];
-          tmem_ld16(tO + c * 16, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st16(tO + c * 16, o);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      // Arrive for tile g only after tile g-2 (same buffer) has been
-      // released by every warp: a warp with no heads in its quarter waits on
-      // nothing else and could otherwise arrive twice in one phase.
-      if (!wwait(bar(kBarPvDone + b), ((g >> 1) & 1u) ^ 1u)) return false;
-      mbar_arrive(bar(kBarOFixed + b));
-      return true;
-    };
-    // Non-owner: the owner's P rows of tile g into TMEM, then release.
-    auto finish_tile = [&](uint32_t g, bool first_of_item) -> bool {
-      const uint32_t b = g & 1u, u = g >> 1;
-      float alpha = 1.f;
-      if (nrow > 0) {
-        if (lane == 0)
-          mbar_arrive_expect_tx(bar(kBarPxFull + 2 * b + slot), static_cast<uint32_t>(nrow * (kTile * 2 + 4)));
-        if (!wwait_cluster(bar(kBarPxFull + 2 * b + slot), u & 1u)) return false;
-        uint32_t pk[kTile / 2];
-        if (valid) {
-#pragma unroll
-          for (int j = 0; j < kTile / 8; ++j)
-            ld_shared_v4(pxbuf(b) + (j * 32 + lane) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-          uint32_t av;
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(av) : "r"(pxabuf(b) + lane * 4) : "memory");
-          alpha = __uint_as_float(av);
-        } else {
-#pragma unroll
-          for (int i = 0; i < kTile / 2; ++i) pk[i] = 0;
-        }
-        tmem_st32(tmem + lane_base + kColP + 32u * b, pk);
-      }
-      return fix_and_release(g, first_of_item, alpha);
-    };
+    // X[b] holds the peer's partial rows of all quarters; a quarter's 32 rows
+    // are 16-byte pieces, piece-major (lane-contiguous), 32 bf16 pairs a row.
+    auto xq = [&](uint32_t b) { return sbase + kOffX + b * kXBytes + q4 * (32 * kTile * 2); };
+    auto xfull = [&](uint32_t b) { return bar(kBarXFull + 4 * b + q4); };
+    auto xfree = [&](uint32_t b) { return bar(kBarXFree + 4 * b + q4); };
     // Epilogue of an item: wait for its last PV, normalise, store.
     auto store_item = [&](const WorkItem& w, uint32_t g_last, float m, float l) -> bool {
       if (!wwait(bar(kBarPvDone + (g_last & 1u)), (g_last >> 1) & 1u)) return false;
       tc_fence_after();
-      if (own && valid) {
+      if (rank == 0 && valid) {
         const float lse2 = m + log2f(l);
         if (w.slot < 0) {
           if (a.lse) a.lse[static_cast<size_t>(w.b) * H + row] = lse2 * 0.69314718055994531f;
@@ -495,9 +422,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       return true;
     };
-    uint32_t g = 0, n_items = 0;
+    uint32_t g = 0;
     bool ok = true;
-    for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
+    for (int it = it_begin; it < it_end && ok; ++it) {
       const WorkItem w = items[it];
       const int lo = max(w.blk_begin * kTile, w.tok_lo);
       const int hi = min(w.blk_end * kTile, w.tok_hi);
@@ -506,119 +433,119 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int base = blk * kTile;
         const uint32_t b = g & 1u, u = g >> 1;
         const bool first_tile = blk == w.blk_begin;
-        uint32_t r[kTile];
-        if (!load_scores(g, r)) { ok = false; break; }
-        if (!own) {
-          // Ship the partial rows once the owner has consumed the previous
-          // ones. Quarters without heads exchange nothing and skip the
-          // handshake (an idle owner would otherwise run phases ahead).
-          if (nrow > 0 && !wwait(bar(kBarXFree + slot), (g & 1u) ^ 1u)) { ok = false; break; }
-          if (valid) {
-            const uint32_t dst = mapa(xbuf, peer);
-            const uint32_t fb = mapa(bar(kBarXFull + slot), peer);
-#pragma unroll
-            for (int j = 0; j < kTile / 4; ++j)
-              st_async_v4(dst + (j * 32 + lane) * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3], fb);
-          }
-          if (!first_tile && !finish_tile(g - 1, blk - 1 == w.blk_begin)) { ok = false; break; }
-          continue;
-        }
-        // Owner: add the peer's partial, then the online softmax.
+        // This rank's partial scores, rounded to bf16 pairs.
+        uint32_t xp[kTile / 2];
+        if (!wwait(bar(kBarSFull + b), u & 1u)) { ok = false; break; }
+        tc_fence_after();
         if (nrow > 0) {
-          if (lane == 0) mbar_arrive_expect_tx(bar(kBarXFull + slot), static_cast<uint32_t>(nrow * kTile * 4));
-          if (!wwait_cluster(bar(kBarXFull + slot), g & 1u)) { ok = false; break; }
+          uint32_t r[kTile];
+#pragma unroll
+          for (int c = 0; c < kTile / 16; ++c) tmem_ld16(tmem + lane_base + kColS + 64u * b + 16 * c, r + 16 * c);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < kTile / 2; ++i) xp[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
         }
+        tc_fence_before();
+        mbar_arrive(bar(kBarSFree + b));
         float alpha = 1.f;
         uint32_t pk[kTile / 2];
-        float s[kTile];
-        if (valid) {
+        if (nrow > 0) {
+          // Ship them once the peer has read what this buffer held two tiles ago.
+          if (!wwait(xfree(b), (u & 1u) ^ 1u)) { ok = false; break; }
+          if (valid) {
+            const uint32_t dst = mapa(xq(b), peer);
+            const uint32_t fb = mapa(xfull(b), peer);
 #pragma unroll
-          for (int j = 0; j < kTile / 4; ++j) {
-            uint32_t x0, x1, x2, x3;
-            ld_shared_v4(xbuf + (j * 32 + lane) * 16, x0, x1, x2, x3);
-            s[4 * j] = __uint_as_float(r[4 * j]) + __uint_as_float(x0);
-            s[4 * j + 1] = __uint_as_float(r[4 * j + 1]) + __uint_as_float(x1);
-            s[4 * j + 2] = __uint_as_float(r[4 * j + 2]) + __uint_as_float(x2);
-            s[4 * j + 3] = __uint_as_float(r[4 * j + 3]) + __uint_as_float(x3);
+            for (int j = 0; j < kTile / 8; ++j)
+              st_async_v4(dst + (j * 32 + lane) * 16, xp[4 * j], xp[4 * j + 1], xp[4 * j + 2], xp[4 * j + 3], fb);
           }
-        }
-        __syncwarp();
-        if (nrow > 0 && lane == 0) mbar_arrive_remote_relaxed(mapa(bar(kBarXFree + slot), peer));  // X consumed
-        if (valid) {
-          float mx = -CUDART_INF_F;
-          if (lo <= base && hi >= base + kTile) {
+          if (lane == 0) mbar_arrive_expect_tx(xfull(b), static_cast<uint32_t>(nrow * kTile * 2));
+          if (!wwait_cluster(xfull(b), u & 1u)) { ok = false; break; }
+          float s[kTile];
+          if (valid) {
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) {
-              s[i] *= a.scale_log2;
-              mx = fmaxf(mx, s[i]);
+            for (int j = 0; j < kTile / 8; ++j) {
+              uint32_t x[4];
+              ld_shared_v4(xq(b) + (j * 32 + lane) * 16, x[0], x[1], x[2], x[3]);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int e = 8 * j + 2 * k;
+                s[e] = __uint_as_float(xp[4 * j + k] << 16) + __uint_as_float(x[k] << 16);
+                s[e + 1] = __uint_as_float(xp[4 * j + k] & 0xffff0000u) + __uint_as_float(x[k] & 0xffff0000u);
+              }
             }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote_relaxed(mapa(xfree(b), peer));  // X[b] read
+          if (valid) {
+            if (lo > base || hi < base + kTile) {
+#pragma unroll
+              for (int i = 0; i < kTile; ++i) {
+                const int pos = base + i;
+                if (pos < lo || pos >= hi) s[i] = -CUDART_INF_F;
+              }
+            }
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int i = 0; i < kTile; ++i) mx = fmaxf(mx, s[i]);
+            mx *= a.scale_log2;
+            if (mx > m + kRescaleThreshold) {
+              alpha = fast_exp2(m - mx);  // 0 on the first tile (m = -inf)
+              l *= alpha;
+              m = mx;
+            }
+            const float neg_m = -m;
+            float rs = 0.f;
+#pragma unroll
+            for (int i = 0; i < kTile / 2; ++i) {
+              const float p0 = fast_exp2(fmaf(s[2 * i], a.scale_log2, neg_m));
+              const float p1 = fast_exp2(fmaf(s[2 * i + 1], a.scale_log2, neg_m));
+              rs += p0 + p1;
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            l += rs;
           } else {
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) {
-              const int pos = base + i;
-              s[i] = (pos >= lo && pos < hi) ? s[i] * a.scale_log2 : -CUDART_INF_F;
-              mx = fmaxf(mx, s[i]);
-            }
+            for (int i = 0; i < kTile / 2; ++i) pk[i] = 0;
           }
-          if (mx > m + kRescaleThreshold) {
-            alpha = fast_exp2(m - mx);  // 0 on the first tile (m = -inf)
-            l *= alpha;
-            m = mx;
-          }
-          float rs = 0.f;
-#pragma unroll
-          for (int i = 0; i < kTile / 2; ++i) {
-            const float p0 = fast_exp2(s[2 * i] - m), p1 = fast_exp2(s[2 * i + 1] - m);
-            rs += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
-          }
-          l += rs;
-        } else {
-#pragma unroll
-          for (int i = 0; i < kTile / 2; ++i) pk[i] = 0;
         }
         // Value rows of this tile outside [lo, hi) may hold anything (stale
         // or unwritten slots): zero this rank's value dims there so that
         // 0 * garbage cannot reach O. QK of the tile is complete here.
         if (lo > base || hi < base + kTile) {
           const uint32_t v0 = sbase + kOffKV + (g % kStages) * kStageBytes;
-          const int t64 = 32 * slot + lane;  // 0..63 over the two owner warps
-          for (int e = t64; e < kTile * kWideChunks * 8; e += 64) {
+          for (int e = 32 * q4 + lane; e < kTile * kWideChunks * 8; e += 128) {
             const int rr = e >> 5, c = (e >> 3) & 3, piece = e & 7;
             const int pos = base + rr;
             if (pos < lo || pos >= hi) st_shared_v4(v0 + c * kWideBytes + rr * 128 + piece * 16, 0, 0, 0, 0);
           }
           fence_proxy_async_smem();
         }
-        // TMEM P[b] and the peer's PX[b] are free once PV(g-2) is done in both ranks.
+        // TMEM P[b] is free once PV(g-2) is done. Waiting here also keeps a
+        // warp without heads from arriving twice in one phase of OFixed.
         if (!wwait(bar(kBarPvDone + b), (u & 1u) ^ 1u)) { ok = false; break; }
-        if (nrow > 0) tmem_st32(tmem + lane_base + kColP + 32u * b, pk);
-        if (valid) {
-          const uint32_t dst = mapa(pxbuf(b), peer);
-          const uint32_t fb = mapa(bar(kBarPxFull + 2 * b + slot), peer);
+        if (nrow > 0) {
+          tmem_st32(tmem + lane_base + kColP + 32u * b, pk);
+          // Rescale this quarter's O rows before PV(g) when the max moved.
+          if (!first_tile && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
+            if (!wwait(bar(kBarPvDone + (b ^ 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }  // PV(g-1) in O
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 256 / 16; ++c) {
+              uint32_t o[16];
+              tmem_ld16(tO + c * 16, o);
+              tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < kTile / 8; ++j)
-            st_async_v4(dst + (j * 32 + lane) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], fb);
-          st_async_b32(mapa(pxabuf(b) + lane * 4, peer), __float_as_uint(alpha), fb);
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st16(tO + c * 16, o);
+            }
+          }
+          tmem_wait_st();
         }
-        if (!fix_and_release(g, first_tile, alpha)) { ok = false; break; }
+        tc_fence_before();
+        mbar_arrive(bar(kBarOFixed + b));
       }
       if (!ok) break;
-      // Row sums to the non-owner; the non-owner finishes its last tile first.
-      if (own) {
-        if (valid) st_async_b32(mapa(l_slot + lane * 4, peer), __float_as_uint(l), mapa(bar(kBarLFull + slot), peer));
-      } else {
-        if (!finish_tile(g - 1, w.blk_end - 1 == w.blk_begin)) { ok = false; break; }
-        if (nrow > 0) {
-          if (lane == 0) mbar_arrive_expect_tx(bar(kBarLFull + slot), static_cast<uint32_t>(nrow * 4));
-          if (!wwait_cluster(bar(kBarLFull + slot), n_items & 1u)) { ok = false; break; }
-        }
-        if (valid) {
-          uint32_t lv;
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(lv) : "r"(l_slot + lane * 4) : "memory");
-          l = __uint_as_float(lv);
-        }
-      }
       if (!store_item(w, g - 1, m, l)) { ok = false; break; }
     }
     if (!ok) {
@@ -626,7 +553,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       flag_status(status, MLA_STATUS_TIMEOUT);
     }
   }
-
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
