@@ -15,24 +15,29 @@
 // moves ~13 bytes/cycle, well below an SM's share of HBM). One work unit is a
 // cluster of two CTAs, rank r, that split the latent dimension evenly:
 //   - rank r holds c_kv[256r, 256r+256) and rope[32r, 32r+32) of every row
-//     (288 dims) and of q; it gathers its slice of each 64-token tile by TMA
-//     (one box per page and chunk, 3-stage ring) and computes a partial
-//     S_r = Q_r K_r^T for all heads with tcgen05.mma M=128 x N=64 into TMEM;
+//     (288 dims) and of q. Per item its q slice goes to TMEM (tcgen05.cp,
+//     staged through two ring slots), so shared memory holds a 5-stage ring
+//     of 64-token tiles gathered by TMA (one box per page and chunk), and
+//     the partial S_r = Q_r K_r^T for all heads comes from tcgen05.mma
+//     M=128 x N=64 with A read from TMEM;
 //   - each rank rounds its partial scores to bf16 and sends them to the
 //     peer (st.async, 16 KB per tile), so both ranks form the same sum
 //     bf16(S_0) + bf16(S_1) (fp32 addition commutes) and run the same online
 //     softmax for all heads (base 2, lazy rescale: the reference max moves
 //     only when the running max grows by more than 8, the final 1/l makes
 //     the result exact), each keeping P in its own TMEM. One exchange per
-//     tile and no P traffic: SM-to-SM bandwidth and latency, not the tensor
-//     pipe, bound this design. The rounding puts a relative error of at most
+//     tile and no P traffic. The rounding puts a relative error of at most
 //     2^-8 of the larger half's partial score on each score;
 //   - each rank accumulates O for all heads over its 256 value dims with
 //     tcgen05.mma M=128 x N=256 x K=64, P read from TMEM and V read MN-major
 //     straight from the gathered tile.
-// Warp roles per CTA (224 threads): warp 0 TMA producer, warp 1 TMEM owner
-// and QK issuer, warps 2-5 exchange / softmax / correction / epilogue (warp
-// w works on TMEM lane quarter w & 3, one head per thread), warp 6 PV issuer.
+// TMEM columns: O [0, 256) fp32, q [256, 400), S [400, 464) fp32, P [464,
+// 496) bf16 pairs; S and P are single-buffered (the next QK waits for S to be
+// read, the next P for the previous PV).
+// Warp roles per CTA (352 threads): warp 0 TMA producer, warp 1 TMEM owner
+// and QK issuer, warps 2-9 exchange / softmax / correction / epilogue (warp
+// w works on TMEM lane quarter w & 3, one head per thread, warps 2-5 on the
+// first 32 tokens of a tile and 6-9 on the last 32), warp 10 PV issuer.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -44,42 +49,49 @@ namespace mla {
 namespace {
 
 constexpr int kTile = kBlockTokens;                 // 64 tokens per tile
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kWideChunks = 4;                      // c_kv chunks of 64 dims per rank
 constexpr int kWideBytes = kTile * 128;             // [64 tokens][64 dims] bf16, 128B swizzle
 constexpr int kNarrowBytes = kTile * 64;            // [64 tokens][32 rope dims], 64B swizzle
 constexpr int kStageBytes = kWideChunks * kWideBytes + kNarrowBytes;   // 36 KB
-constexpr int kQWideBytes = 128 * 128;              // [128 heads][64 dims]
-constexpr int kQNarrowBytes = 128 * 64;             // [128 heads][32 rope dims]
-constexpr int kQBytes = kWideChunks * kQWideBytes + kQNarrowBytes;     // 72 KB
+constexpr int kQWideBytes = 128 * 128;              // [128 heads][64 dims], 16 KB
+constexpr int kQNarrowBytes = 128 * 64;             // [128 heads][32 rope dims], 8 KB
 constexpr int kXBytes = 128 * kTile * 2;            // the peer's partial S of 128 rows, bf16
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffQn = 0;                           // q rope part, staged for TMEM
+constexpr int kOffKV = kOffQn + kQNarrowBytes;
 constexpr int kOffX = kOffKV + kStages * kStageBytes;  // [2 buffers]
-constexpr int kOffBar = kOffX + 2 * kXBytes;
+constexpr int kOffRed = kOffX + 2 * kXBytes;       // [2 tile parities][4 quarters][2 halves][32] fp32
+constexpr int kOffLRed = kOffRed + 2048;            // [4 quarters][2 halves][32] fp32
+constexpr int kOffBar = kOffLRed + 1024;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;    // barriers + alignment slack
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;
+constexpr int kPvWarp = 10;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0;                       // O: [0, 256)
-constexpr uint32_t kColS = 256;                     // S[b]: 256 + 64 b
-constexpr uint32_t kColP = 384;                     // P[b]: 384 + 32 b (bf16 pairs)
+constexpr uint32_t kColO = 0;                       // O: [0, 256) fp32
+constexpr uint32_t kColQ = 256;                     // q: [256, 400) bf16 pairs (wide 128 + rope 16)
+constexpr uint32_t kColS = 400;                     // S: [400, 464) fp32
+constexpr uint32_t kColP = 464;                     // P: [464, 496) bf16 pairs
 constexpr float kRescaleThreshold = 8.0f;
 
 static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0 && kOffX % 1024 == 0, "alignment");
+static_assert(2 * kQWideBytes <= kStageBytes, "a ring slot holds two wide q chunks");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 enum Bar {
   kBarKvFull = 0,                  // [kStages]
   kBarKvEmpty = kBarKvFull + kStages,
-  kBarQFull = kBarKvEmpty + kStages,
-  kBarQFree,
-  kBarSFull,                       // [2]
-  kBarSFree = kBarSFull + 2,       // [2]
-  kBarXFull = kBarSFree + 2,       // [2 buffers][4 quarters]: the peer's partial rows landed
-  kBarXFree = kBarXFull + 8,       // [2 buffers][4 quarters]: the peer read this rank's partial rows
-  kBarOFixed = kBarXFree + 8,      // [2] P in TMEM and O rescaled for this tile
-  kBarPvDone = kBarOFixed + 2,     // [2] PV on that buffer done
-  kBarDrain = kBarPvDone + 2,
+  kBarQnFull = kBarKvEmpty + kStages,  // q rope part landed
+  kBarQnFree,                      // q rope part copied into TMEM
+  kBarQDone,                       // every QK of the item complete: TMEM q may be replaced
+  kBarSFull,
+  kBarSFree,
+  kBarXFull,                       // [2 buffers][4 quarters][2 halves]: the peer's partial rows landed
+  kBarXFree = kBarXFull + 16,      // [2 buffers][4 quarters][2 halves]: the peer read this rank's partial rows
+  kBarPairMax = kBarXFree + 16,    // [4 quarters]: both halves' row maxima of the tile posted
+  kBarPairSum = kBarPairMax + 4,   // [4 quarters]: both halves' row sums of the item posted
+  kBarOFixed = kBarPairSum + 4,    // P in TMEM and O rescaled for this tile
+  kBarPvDone,                      // PV of the tile done
+  kBarDrain,
   kBarDrainPv,
   kNumBars
 };
@@ -146,15 +158,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarKvFull + i), 1);
       mbar_init(bar(kBarKvEmpty + i), 1);
     }
-    mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQFree), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarSFull + i), 1);
-      mbar_init(bar(kBarSFree + i), 128);
-      mbar_init(bar(kBarOFixed + i), 128);
-      mbar_init(bar(kBarPvDone + i), 1);
+    mbar_init(bar(kBarQnFull), 1);
+    mbar_init(bar(kBarQnFree), 1);
+    mbar_init(bar(kBarQDone), 1);
+    mbar_init(bar(kBarSFull), 1);
+    mbar_init(bar(kBarSFree), 256);
+    mbar_init(bar(kBarOFixed), 256);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(kBarPairMax + i), 64);
+      mbar_init(bar(kBarPairSum + i), 64);
     }
-    for (int i = 0; i < 8; ++i) {
+    mbar_init(bar(kBarPvDone), 1);
+    for (int i = 0; i < 16; ++i) {
       mbar_init(bar(kBarXFull + i), 1);
       mbar_init(bar(kBarXFree + i), 1);
     }
@@ -180,6 +195,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int wide_x = 256 * static_cast<int>(rank);        // first c_kv dim of this rank
   const int narrow_x = 512 + 32 * static_cast<int>(rank);  // first rope dim of this rank
 
+  // Ring slots: every item takes two slots for its q (wide chunks 0-1 and
+  // 2-3, 16 KB each, on their way to TMEM), then one slot per 64-token tile.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp walks the tiles; lane 0 issues the copies. Page ids are
@@ -190,8 +207,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int oob_row = a.num_layers * a.num_pages * ps;  // reads as zeros
     const int rows_per_box = ps < kTile ? ps : kTile;
     const int boxes = kTile / rows_per_box;
-    uint32_t g = 0;
-    int last_q_item = -1;
+    uint32_t sl = 0;  // ring slot
+    int last_qn_item = -1;
     uint32_t n_items = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
@@ -202,17 +219,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int32_t* ids = a.page_indptr ? a.page_ids + a.page_indptr[w.b]
                                          : a.page_ids + static_cast<int64_t>(w.b) * a.max_blocks;
       int batch0 = -64, my_id = -1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQFree), (n_items & 1u) ^ 1u, abort_flag));
+      // q of this item: wide chunks through two ring slots, the rope part
+      // into its own buffer once the previous item's copy into TMEM is done.
+      for (int h = 0; h < 2 && ok; ++h, ++sl) {
+        const uint32_t stage = sl % kStages, use = sl / kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarKvEmpty + stage), (use & 1u) ^ 1u, abort_flag));
+        if (ok && lane == 0) {
+          const uint32_t fb = bar(kBarKvFull + stage);
+          mbar_arrive_expect_tx(fb, 2 * kQWideBytes);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(sbase + kOffKV + stage * kStageBytes + c * kQWideBytes, &p.q_wide, fb,
+                        wide_x + 64 * (2 * h + c), w.b * H);
+        }
+      }
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQnFree), (n_items & 1u) ^ 1u, abort_flag));
       if (!ok) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kBarQFull), kQBytes);
-        for (int c = 0; c < kWideChunks; ++c)
-          tma_load_2d(sbase + kOffQ + c * kQWideBytes, &p.q_wide, bar(kBarQFull), wide_x + 64 * c, w.b * H);
-        tma_load_2d(sbase + kOffQ + kWideChunks * kQWideBytes, &p.q_narrow, bar(kBarQFull), narrow_x, w.b * H);
+        mbar_arrive_expect_tx(bar(kBarQnFull), kQNarrowBytes);
+        tma_load_2d(sbase + kOffQn, &p.q_narrow, bar(kBarQnFull), narrow_x, w.b * H);
       }
-      last_q_item = static_cast<int>(n_items);
-      for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++g) {
-        const uint32_t stage = g % kStages, use = g / kStages;
+      last_qn_item = static_cast<int>(n_items);
+      for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++sl) {
+        const uint32_t stage = sl % kStages, use = sl / kStages;
         int rows[4];
         int nbox = 0;
 #pragma unroll
@@ -268,43 +297,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (*abort_flag) {
         // Let every copy already issued land before the CTA can exit.
-        for (uint32_t k = (g > kStages ? g - kStages : 0); k < g; ++k)
+        for (uint32_t k = (sl > kStages ? sl - kStages : 0); k < sl; ++k)
           mbar_wait(bar(kBarKvFull + k % kStages), (k / kStages) & 1u, nullptr);
-        if (last_q_item >= 0) mbar_wait(bar(kBarQFull), last_q_item & 1, nullptr);
+        if (last_qn_item >= 0) mbar_wait(bar(kBarQnFull), last_qn_item & 1, nullptr);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
+    // Per item: once the previous item's QK is complete, copy q into TMEM
+    // (tcgen05.cp, wide part 128 columns + rope part 16 columns); per tile:
+    // S = q K^T with A read from TMEM (TS form), so shared memory streams
+    // only the K tile through the tensor core.
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16(128, kTile, false, false);
-      uint32_t g = 0, n_items = 0;
+      const uint32_t tQ = tmem + kColQ;
+      const uint32_t tS = tmem + kColS;
+      uint32_t sl = 0, g = 0, n_items = 0;
       bool ok = true;
       for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
         const WorkItem w = items[it];
         const int nt = w.blk_end - w.blk_begin;
-        if (!mbar_wait(bar(kBarQFull), n_items & 1u, abort_flag)) { ok = false; break; }
+        const uint32_t s0 = sl % kStages, s1 = (sl + 1) % kStages;
+        if (!mbar_wait(bar(kBarKvFull + s0), (sl / kStages) & 1u, abort_flag) ||
+            !mbar_wait(bar(kBarKvFull + s1), ((sl + 1) / kStages) & 1u, abort_flag) ||
+            !mbar_wait(bar(kBarQnFull), n_items & 1u, abort_flag) ||
+            !mbar_wait(bar(kBarQDone), (n_items & 1u) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        for (int t = 0; t < nt; ++t, ++g) {
-          const uint32_t stage = g % kStages, use = g / kStages;
-          const uint32_t b = g & 1u, u = g >> 1;
+#pragma unroll
+        for (int c = 0; c < kWideChunks; ++c) {
+          const uint32_t src = sbase + kOffKV + ((c < 2) ? s0 : s1) * kStageBytes + (c & 1) * kQWideBytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tmem_cp_128x256b(tQ + 8u * (4 * c + k), sdesc_sw128(src + k * 32, 16, 1024));
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) tmem_cp_128x256b(tQ + 128u + 8u * k, sdesc_sw64(sbase + kOffQn + k * 32, 512));
+        mma_commit(bar(kBarKvEmpty + s0));
+        mma_commit(bar(kBarKvEmpty + s1));
+        mma_commit(bar(kBarQnFree));
+        sl += 2;
+        for (int t = 0; t < nt; ++t, ++g, ++sl) {
+          const uint32_t stage = sl % kStages, use = sl / kStages;
           if (!mbar_wait(bar(kBarKvFull + stage), use & 1u, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(bar(kBarSFree + b), (u & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar(kBarSFree), (g & 1u) ^ 1u, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t kv = sbase + kOffKV + stage * kStageBytes;
-          const uint32_t tS = tmem + kColS + 64u * b;
 #pragma unroll
           for (int c = 0; c < kWideChunks; ++c)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_bf16_ss(tS, sdesc_sw128(sbase + kOffQ + c * kQWideBytes + k * 32, 16, 1024),
-                          sdesc_sw128(kv + c * kWideBytes + k * 32, 16, 1024), idesc_qk, (c | k) != 0);
+              mma_bf16_ts(tS, tQ + 8u * (4 * c + k), sdesc_sw128(kv + c * kWideBytes + k * 32, 16, 1024), idesc_qk,
+                          (c | k) != 0);
 #pragma unroll
           for (int k = 0; k < 2; ++k)
-            mma_bf16_ss(tS, sdesc_sw64(sbase + kOffQ + kWideChunks * kQWideBytes + k * 32, 512),
-                        sdesc_sw64(kv + kWideChunks * kWideBytes + k * 32, 512), idesc_qk, 1u);
-          mma_commit(bar(kBarSFull + b));
+            mma_bf16_ts(tS, tQ + 128u + 8u * k, sdesc_sw64(kv + kWideChunks * kWideBytes + k * 32, 512), idesc_qk,
+                        1u);
+          mma_commit(bar(kBarSFull));
         }
-        if (ok) mma_commit(bar(kBarQFree));  // every QK of this item issued
+        if (ok) mma_commit(bar(kBarQDone));  // every QK of this item complete: q may be replaced
       }
       if (!ok) {
         *abort_flag = 1;
@@ -313,28 +365,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mma_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, nullptr);
     }
-  } else if (warp == 6) {
+  } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV issuer
     if (lane == 0) {
       const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
       const uint32_t tO = tmem + kColO;
-      uint32_t g = 0;
+      uint32_t sl = 0, g = 0;
       bool ok = true;
       for (int it = it_begin; it < it_end && ok; ++it) {
         const WorkItem w = items[it];
         const int nt = w.blk_end - w.blk_begin;
-        for (int t = 0; t < nt; ++t, ++g) {
-          const uint32_t b = g & 1u, u = g >> 1;
-          if (!mbar_wait(bar(kBarOFixed + b), u & 1u, abort_flag)) { ok = false; break; }
+        sl += 2;
+        for (int t = 0; t < nt; ++t, ++g, ++sl) {
+          if (!mbar_wait(bar(kBarOFixed), g & 1u, abort_flag)) { ok = false; break; }
           tc_fence_after();
           fence_proxy_async_smem();
-          const uint32_t v0 = sbase + kOffKV + (g % kStages) * kStageBytes;
+          const uint32_t v0 = sbase + kOffKV + (sl % kStages) * kStageBytes;
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ts(tO, tmem + kColP + 32u * b + 8u * k, sdesc_sw128(v0 + k * 16 * 128, kWideBytes, 1024),
-                        idesc_pv, (t | k) != 0);
-          mma_commit(bar(kBarKvEmpty + g % kStages));
-          mma_commit(bar(kBarPvDone + b));
+            mma_bf16_ts(tO, tmem + kColP + 8u * k, sdesc_sw128(v0 + k * 16 * 128, kWideBytes, 1024), idesc_pv,
+                        (t | k) != 0);
+          mma_commit(bar(kBarKvEmpty + sl % kStages));
+          mma_commit(bar(kBarPvDone));
         }
       }
       if (!ok) {
@@ -344,41 +396,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mma_commit(bar(kBarDrainPv));
       mbar_wait(bar(kBarDrainPv), 0, nullptr);
     }
-  } else {
+  } else if (warp != kPvWarp) {
     // ------------------------------------------------------------ exchange, softmax, correction, epilogue
-    // Warp w works on TMEM lane quarter q4 = w & 3: rows (heads) 32 q4 + lane,
-    // one head per thread. Per tile g: this rank's partial scores of the
-    // quarter, rounded to bf16, go to the peer (st.async, 4 KB) and the
+    // Two warps per TMEM lane quarter q4 = w & 3 (rows / heads 32 q4 + lane,
+    // one head per thread): warps 2-5 take tokens [0, 32) of every tile and
+    // warps 6-9 tokens [32, 64), so each SM sub-partition runs two of them
+    // and hides one's latencies behind the other. Per tile g: this rank's
+    // partial scores, rounded to bf16, go to the peer (st.async) and the
     // peer's arrive the same way; both ranks then form the same sum
-    // bf16(S_0) + bf16(S_1) (fp32 addition commutes), so both run the same
-    // online softmax (base 2, lazy rescale: the reference max moves only
-    // when the running max grows by more than 8; the final 1/l keeps the
-    // result exact) and keep the same P in their own TMEM. One exchange per
-    // tile, no P traffic, and every SM sub-partition takes a quarter of the
-    // exponentials.
+    // bf16(S_0) + bf16(S_1) (fp32 addition commutes), the two halves of a
+    // row agree on its running max through shared memory, and both ranks
+    // run the same online softmax and keep the same P in their own TMEM.
     const int q4 = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int nrow = min(max(H - 32 * q4, 0), 32);  // valid heads in this quarter
     const int row = 32 * q4 + lane;                 // head of this lane
     const bool valid = lane < nrow;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-    const uint32_t tO = tmem + lane_base + kColO;
-    const uint32_t dim0 = 256u * rank;
+    const uint32_t tO = tmem + lane_base + kColO + 128u * half;  // this warp's half of O
+    const uint32_t dim0 = 256u * rank + 128u * half;
+    constexpr int kHalf = kTile / 2;
     auto wwait = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(b, parity, abort_flag));
     };
     auto wwait_cluster = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait<true>(b, parity, abort_flag));
     };
-    // X[b] holds the peer's partial rows of all quarters; a quarter's 32 rows
-    // are 16-byte pieces, piece-major (lane-contiguous), 32 bf16 pairs a row.
-    auto xq = [&](uint32_t b) { return sbase + kOffX + b * kXBytes + q4 * (32 * kTile * 2); };
-    auto xfull = [&](uint32_t b) { return bar(kBarXFull + 4 * b + q4); };
-    auto xfree = [&](uint32_t b) { return bar(kBarXFree + 4 * b + q4); };
-    // Epilogue of an item: wait for its last PV, normalise, store.
+    // X[b]: the peer's partial rows; per quarter and half 32 rows of 32
+    // tokens as 16-byte pieces, piece-major (lane-contiguous).
+    auto xq = [&](uint32_t b) { return sbase + kOffX + b * kXBytes + q4 * (32 * kTile * 2) + half * (32 * kHalf * 2); };
+    auto xfull = [&](uint32_t b) { return bar(kBarXFull + 8 * b + 2 * q4 + half); };
+    auto xfree = [&](uint32_t b) { return bar(kBarXFree + 8 * b + 2 * q4 + half); };
+    // Row maxima / row sums handed between the two warps of a quarter.
+    auto red = [&](uint32_t par, int h) { return sbase + kOffRed + par * 1024 + q4 * 256 + h * 128 + lane * 4; };
+    auto lred = [&](int h) { return sbase + kOffLRed + q4 * 256 + h * 128 + lane * 4; };
+    // Epilogue of an item: wait for its last PV, normalise this warp's 128
+    // value dims, store.
     auto store_item = [&](const WorkItem& w, uint32_t g_last, float m, float l) -> bool {
-      if (!wwait(bar(kBarPvDone + (g_last & 1u)), (g_last >> 1) & 1u)) return false;
+      if (!wwait(bar(kBarPvDone), g_last & 1u)) return false;
       tc_fence_after();
-      if (rank == 0 && valid) {
+      if (rank == 0 && half == 0 && valid) {
         const float lse2 = m + log2f(l);
         if (w.slot < 0) {
           if (a.lse) a.lse[static_cast<size_t>(w.b) * H + row] = lse2 * 0.69314718055994531f;
@@ -389,7 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (nrow > 0) {
         const float inv_l = valid ? 1.f / l : 0.f;
 #pragma unroll 1
-        for (int c = 0; c < 256 / 32; ++c) {
+        for (int c = 0; c < 128 / 32; ++c) {
           uint32_t o[32];
           tmem_ld16(tO + c * 32, o);
           tmem_ld16(tO + c * 32 + 16, o + 16);
@@ -422,49 +479,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       return true;
     };
-    uint32_t g = 0;
+    // Software pipeline: the partial scores of tile g+1 are fetched from TMEM
+    // and shipped before the softmax of tile g, so the transfer to the peer
+    // overlaps the exponentials instead of sitting in this loop.
+    int total_tiles = 0;
+    for (int it = it_begin; it < it_end; ++it) total_tiles += items[it].blk_end - items[it].blk_begin;
+    // Wait for S(gg), keep this rank's partial (this warp's 32 tokens) as
+    // bf16 pairs in xp, release S, and send the pairs to the peer once it
+    // has read that buffer's previous contents.
+    auto fetch = [&](uint32_t gg, uint32_t* xp) -> bool {
+      const uint32_t b = gg & 1u, u = gg >> 1;
+      if (!wwait(bar(kBarSFull), gg & 1u)) return false;
+      tc_fence_after();
+      if (nrow > 0) {
+        uint32_t r[kHalf];
+        tmem_ld16(tmem + lane_base + kColS + kHalf * half, r);
+        tmem_ld16(tmem + lane_base + kColS + kHalf * half + 16, r + 16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < kHalf / 2; ++i) xp[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kBarSFree));
+      if (nrow > 0) {
+        if (!wwait(xfree(b), (u & 1u) ^ 1u)) return false;
+        if (valid) {
+          const uint32_t dst = mapa(xq(b), peer);
+          const uint32_t fb = mapa(xfull(b), peer);
+#pragma unroll
+          for (int j = 0; j < kHalf / 8; ++j)
+            st_async_v4(dst + (j * 32 + lane) * 16, xp[4 * j], xp[4 * j + 1], xp[4 * j + 2], xp[4 * j + 3], fb);
+        }
+        if (lane == 0) mbar_arrive_expect_tx(xfull(b), static_cast<uint32_t>(nrow * kHalf * 2));
+      }
+      return true;
+    };
+    uint32_t g = 0, sl = 0, n_items = 0;
     bool ok = true;
-    for (int it = it_begin; it < it_end && ok; ++it) {
+    uint32_t xp[kHalf / 2];
+    if (total_tiles > 0) ok = fetch(0, xp);
+    for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
       const WorkItem w = items[it];
       const int lo = max(w.blk_begin * kTile, w.tok_lo);
       const int hi = min(w.blk_end * kTile, w.tok_hi);
-      float m = -CUDART_INF_F, l = 0.f;
-      for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++g) {
-        const int base = blk * kTile;
+      float m = -CUDART_INF_F, l = 0.f;  // l: this warp's tokens only
+      sl += 2;  // the item's q slots
+      for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++g, ++sl) {
+        const int base = blk * kTile + kHalf * half;  // first token of this warp
         const uint32_t b = g & 1u, u = g >> 1;
         const bool first_tile = blk == w.blk_begin;
-        // This rank's partial scores, rounded to bf16 pairs.
-        uint32_t xp[kTile / 2];
-        if (!wwait(bar(kBarSFull + b), u & 1u)) { ok = false; break; }
-        tc_fence_after();
-        if (nrow > 0) {
-          uint32_t r[kTile];
-#pragma unroll
-          for (int c = 0; c < kTile / 16; ++c) tmem_ld16(tmem + lane_base + kColS + 64u * b + 16 * c, r + 16 * c);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < kTile / 2; ++i) xp[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-        }
-        tc_fence_before();
-        mbar_arrive(bar(kBarSFree + b));
+        uint32_t xp_next[kHalf / 2];
+        if (static_cast<int>(g) + 1 < total_tiles && !fetch(g + 1, xp_next)) { ok = false; break; }
         float alpha = 1.f;
-        uint32_t pk[kTile / 2];
+        uint32_t pk[kHalf / 2];
         if (nrow > 0) {
-          // Ship them once the peer has read what this buffer held two tiles ago.
-          if (!wwait(xfree(b), (u & 1u) ^ 1u)) { ok = false; break; }
-          if (valid) {
-            const uint32_t dst = mapa(xq(b), peer);
-            const uint32_t fb = mapa(xfull(b), peer);
-#pragma unroll
-            for (int j = 0; j < kTile / 8; ++j)
-              st_async_v4(dst + (j * 32 + lane) * 16, xp[4 * j], xp[4 * j + 1], xp[4 * j + 2], xp[4 * j + 3], fb);
-          }
-          if (lane == 0) mbar_arrive_expect_tx(xfull(b), static_cast<uint32_t>(nrow * kTile * 2));
           if (!wwait_cluster(xfull(b), u & 1u)) { ok = false; break; }
-          float s[kTile];
+          float s[kHalf];
+          float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
           if (valid) {
 #pragma unroll
-            for (int j = 0; j < kTile / 8; ++j) {
+            for (int j = 0; j < kHalf / 8; ++j) {
               uint32_t x[4];
               ld_shared_v4(xq(b) + (j * 32 + lane) * 16, x[0], x[1], x[2], x[3]);
 #pragma unroll
@@ -478,60 +552,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_remote_relaxed(mapa(xfree(b), peer));  // X[b] read
           if (valid) {
-            if (lo > base || hi < base + kTile) {
+            if (lo > base || hi < base + kHalf) {
 #pragma unroll
-              for (int i = 0; i < kTile; ++i) {
+              for (int i = 0; i < kHalf; ++i) {
                 const int pos = base + i;
                 if (pos < lo || pos >= hi) s[i] = -CUDART_INF_F;
               }
             }
-            float mx = -CUDART_INF_F;
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) mx = fmaxf(mx, s[i]);
-            mx *= a.scale_log2;
+            for (int i = 0; i < kHalf; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+          }
+          // The row max over both halves (scores are scaled by a positive
+          // factor, so the max of the raw sums is taken).
+          const float mx_half = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          st_shared_f32(red(g & 1u, half), mx_half);
+          mbar_arrive(bar(kBarPairMax + q4));
+          if (!wwait(bar(kBarPairMax + q4), g & 1u)) { ok = false; break; }
+          if (valid) {
+            const float mx = fmaxf(mx_half, ld_shared_f32(red(g & 1u, half ^ 1))) * a.scale_log2;
             if (mx > m + kRescaleThreshold) {
               alpha = fast_exp2(m - mx);  // 0 on the first tile (m = -inf)
               l *= alpha;
               m = mx;
             }
             const float neg_m = -m;
-            float rs = 0.f;
+            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < kTile / 2; ++i) {
+            for (int i = 0; i < kHalf / 2; ++i) {
               const float p0 = fast_exp2(fmaf(s[2 * i], a.scale_log2, neg_m));
               const float p1 = fast_exp2(fmaf(s[2 * i + 1], a.scale_log2, neg_m));
-              rs += p0 + p1;
+              rs4[i & 3] += p0 + p1;
               pk[i] = pack_bf16x2(p0, p1);
             }
-            l += rs;
+            l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
           } else {
 #pragma unroll
-            for (int i = 0; i < kTile / 2; ++i) pk[i] = 0;
+            for (int i = 0; i < kHalf / 2; ++i) pk[i] = 0;
           }
         }
+#pragma unroll
+        for (int i = 0; i < kHalf / 2; ++i) xp[i] = xp_next[i];
         // Value rows of this tile outside [lo, hi) may hold anything (stale
         // or unwritten slots): zero this rank's value dims there so that
         // 0 * garbage cannot reach O. QK of the tile is complete here.
-        if (lo > base || hi < base + kTile) {
-          const uint32_t v0 = sbase + kOffKV + (g % kStages) * kStageBytes;
-          for (int e = 32 * q4 + lane; e < kTile * kWideChunks * 8; e += 128) {
+        const int tbase = blk * kTile;
+        if (lo > tbase || hi < tbase + kTile) {
+          const uint32_t v0 = sbase + kOffKV + (sl % kStages) * kStageBytes;
+          for (int e = 32 * q4 + 128 * half + lane; e < kTile * kWideChunks * 8; e += 256) {
             const int rr = e >> 5, c = (e >> 3) & 3, piece = e & 7;
-            const int pos = base + rr;
+            const int pos = tbase + rr;
             if (pos < lo || pos >= hi) st_shared_v4(v0 + c * kWideBytes + rr * 128 + piece * 16, 0, 0, 0, 0);
           }
           fence_proxy_async_smem();
         }
-        // TMEM P[b] is free once PV(g-2) is done. Waiting here also keeps a
-        // warp without heads from arriving twice in one phase of OFixed.
-        if (!wwait(bar(kBarPvDone + b), (u & 1u) ^ 1u)) { ok = false; break; }
+        // TMEM P and O are free once PV(g-1) is done. Waiting here also keeps
+        // a warp without heads from arriving twice in one phase of OFixed.
+        if (!wwait(bar(kBarPvDone), (g & 1u) ^ 1u)) { ok = false; break; }
+        tc_fence_after();
         if (nrow > 0) {
-          tmem_st32(tmem + lane_base + kColP + 32u * b, pk);
-          // Rescale this quarter's O rows before PV(g) when the max moved.
+          tmem_st16(tmem + lane_base + kColP + (kHalf / 2) * half, pk);
+          // Rescale this warp's half of the quarter's O rows before PV(g)
+          // when the max moved (both halves see the same alpha).
           if (!first_tile && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
-            if (!wwait(bar(kBarPvDone + (b ^ 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }  // PV(g-1) in O
-            tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < 256 / 16; ++c) {
+            for (int c = 0; c < 128 / 16; ++c) {
               uint32_t o[16];
               tmem_ld16(tO + c * 16, o);
               tmem_wait_ld();
@@ -543,9 +627,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(bar(kBarOFixed + b));
+        mbar_arrive(bar(kBarOFixed));
       }
       if (!ok) break;
+      // The row sum over both halves.
+      if (nrow > 0) {
+        st_shared_f32(lred(half), l);
+        mbar_arrive(bar(kBarPairSum + q4));
+        if (!wwait(bar(kBarPairSum + q4), n_items & 1u)) { ok = false; break; }
+        l += ld_shared_f32(lred(half ^ 1));
+      }
       if (!store_item(w, g - 1, m, l)) { ok = false; break; }
     }
     if (!ok) {
@@ -553,6 +644,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       flag_status(status, MLA_STATUS_TIMEOUT);
     }
   }
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
