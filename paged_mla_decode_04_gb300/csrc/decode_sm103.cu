@@ -49,7 +49,7 @@ namespace mla {
 namespace {
 
 constexpr int kTile = kBlockTokens;                 // 64 tokens per tile
-constexpr int kStages = 5;
+constexpr int kMaxStages = 5;
 constexpr int kWideChunks = 4;                      // c_kv chunks of 64 dims per rank
 constexpr int kWideBytes = kTile * 128;             // [64 tokens][64 dims] bf16, 128B swizzle
 constexpr int kNarrowBytes = kTile * 64;            // [64 tokens][32 rope dims], 64B swizzle
@@ -57,15 +57,32 @@ constexpr int kStageBytes = kWideChunks * kWideBytes + kNarrowBytes;   // 36 KB
 constexpr int kQWideBytes = 128 * 128;              // [128 heads][64 dims], 16 KB
 constexpr int kQNarrowBytes = 128 * 64;             // [128 heads][32 rope dims], 8 KB
 constexpr int kXBytes = 128 * kTile * 2;            // the peer's partial S of 128 rows, bf16
-constexpr int kOffQn = 0;                           // q rope part, staged for TMEM
-constexpr int kOffKV = kOffQn + kQNarrowBytes;
-constexpr int kOffX = kOffKV + kStages * kStageBytes;  // [2 buffers]
-constexpr int kOffRed = kOffX + 2 * kXBytes;       // [2 tile parities][4 quarters][2 halves][32] fp32
-constexpr int kOffLRed = kOffRed + 2048;            // [4 quarters][2 halves][32] fp32
-constexpr int kOffBar = kOffLRed + 1024;
-constexpr int kSmemBytes = kOffBar + 512 + 1024;    // barriers + alignment slack
-constexpr int kThreads = 352;
+constexpr int kF8WideBytes = kTile * 256;           // fp8 tile: [64 tokens][256 c_kv dims], unswizzled
+constexpr int kF8Bytes = kF8WideBytes + kTile * 32;  // + [64 tokens][32 rope dims]
+constexpr int kF8Stages = 4;
 constexpr int kPvWarp = 10;
+constexpr int kCvtWarp0 = 11;                       // fp8 pools: warps 11-14 widen fp8 tiles to f16
+
+// Shared-memory plan of the two variants. bf16 pools: q rope part | 5-stage
+// ring of bf16 tiles | exchange | reductions | barriers. fp8 pools: the ring
+// holds the widened f16 tiles (3 stages) and a 4-stage ring of raw fp8 tiles
+// sits beside it.
+template <bool kFp8>
+struct Cfg {
+  static constexpr int kStages = kFp8 ? 3 : 5;
+  static constexpr int kOffQn = 0;                            // q rope part, staged for TMEM
+  static constexpr int kOffKV = kOffQn + kQNarrowBytes;
+  static constexpr int kOffF8 = kOffKV + kStages * kStageBytes;
+  static constexpr int kOffX = kOffF8 + (kFp8 ? kF8Stages * kF8Bytes : 0);  // [2 buffers]
+  static constexpr int kOffRed = kOffX + 2 * kXBytes;  // [2 tile parities][4 quarters][2 halves][32] fp32
+  static constexpr int kOffLRed = kOffRed + 2048;      // [4 quarters][2 halves][32] fp32
+  static constexpr int kOffBar = kOffLRed + 1024;
+  static constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // barriers + alignment slack
+  static constexpr int kThreads = kFp8 ? 480 : 352;
+  static_assert(kOffKV % 1024 == 0 && kOffF8 % 1024 == 0 && kOffX % 1024 == 0, "alignment");
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kStages <= kMaxStages, "barrier arrays");
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                       // O: [0, 256) fp32
 constexpr uint32_t kColQ = 256;                     // q: [256, 400) bf16 pairs (wide 128 + rope 16)
@@ -73,14 +90,17 @@ constexpr uint32_t kColS = 400;                     // S: [400, 464) fp32
 constexpr uint32_t kColP = 464;                     // P: [464, 496) bf16 pairs
 constexpr float kRescaleThreshold = 8.0f;
 
-static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0 && kOffX % 1024 == 0, "alignment");
+static_assert(kStageBytes % 1024 == 0 && kF8Bytes % 1024 == 0, "alignment");
 static_assert(2 * kQWideBytes <= kStageBytes, "a ring slot holds two wide q chunks");
-static_assert(kSmemBytes <= 232448, "shared memory");
 
 enum Bar {
-  kBarKvFull = 0,                  // [kStages]
-  kBarKvEmpty = kBarKvFull + kStages,
-  kBarQnFull = kBarKvEmpty + kStages,  // q rope part landed
+  kBarKvFull = 0,                  // [stages] tile (or q chunks) ready for the tensor core
+  kBarKvEmpty = kBarKvFull + kMaxStages,
+  kBarRawQ = kBarKvEmpty + kMaxStages,     // [2] fp8 pools: the item's bf16 q chunks landed, not yet f16
+  kBarF8Full = kBarRawQ + 2,               // [kF8Stages] fp8 tile landed
+  kBarF8Empty = kBarF8Full + kF8Stages,    // [kF8Stages] fp8 tile widened
+  kBarQnFull = kBarF8Empty + kF8Stages,    // q rope part ready
+  kBarQnRaw,                       // fp8 pools: q rope part landed, not yet f16
   kBarQnFree,                      // q rope part copied into TMEM
   kBarQDone,                       // every QK of the item complete: TMEM q may be replaced
   kBarSFull,
@@ -95,11 +115,11 @@ enum Bar {
   kBarDrainPv,
   kNumBars
 };
-static_assert(kNumBars * 8 + 8 <= 512, "barrier area");
+static_assert(kNumBars * 8 + 8 <= 1024, "barrier area");
 
 struct Params {
-  CUtensorMap kv_wide;    // pool rows [NL*P*ps][576] bf16, box {64, rows}, 128B swizzle
-  CUtensorMap kv_narrow;  // same rows, box {32, rows}, 64B swizzle
+  CUtensorMap kv_wide;    // pool rows [NL*P*ps][576]: bf16 box {64, rows} 128B swizzle; fp8 box {256, rows}
+  CUtensorMap kv_narrow;  // same rows: bf16 box {32, rows} 64B swizzle; fp8 box {32, rows}
   CUtensorMap q_wide;     // q rows [B*H][576] bf16, box {64, 128}, 128B swizzle
   CUtensorMap q_narrow;   // box {32, 128}, 64B swizzle
   DecodeArgs a;
@@ -119,8 +139,21 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   tmem_st16(taddr + 16, r + 16);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<kFp8>;
+  constexpr int kStages = C::kStages;
+  constexpr int kOffQn = C::kOffQn;
+  constexpr int kOffKV = C::kOffKV;
+  constexpr int kOffF8 = C::kOffF8;
+  constexpr int kOffX = C::kOffX;
+  constexpr int kOffRed = C::kOffRed;
+  constexpr int kOffLRed = C::kOffLRed;
+  constexpr int kOffBar = C::kOffBar;
+  // fp8 pools run the tensor core on f16 (q and P converted, codes exact).
+  constexpr uint32_t kIdescQk = kFp8 ? idesc_f16(128, kTile, false, false) : idesc_bf16(128, kTile, false, false);
+  constexpr uint32_t kIdescPv = kFp8 ? idesc_f16(128, 256, false, true) : idesc_bf16(128, 256, false, true);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
@@ -155,10 +188,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kBarKvFull + i), 1);
+      mbar_init(bar(kBarKvFull + i), kFp8 ? 128 : 1);  // fp8: every converter thread arrives
       mbar_init(bar(kBarKvEmpty + i), 1);
     }
-    mbar_init(bar(kBarQnFull), 1);
+    mbar_init(bar(kBarRawQ), 1);
+    mbar_init(bar(kBarRawQ + 1), 1);
+    for (int i = 0; i < kF8Stages; ++i) {
+      mbar_init(bar(kBarF8Full + i), 1);
+      mbar_init(bar(kBarF8Empty + i), 128);
+    }
+    mbar_init(bar(kBarQnFull), kFp8 ? 128 : 1);
+    mbar_init(bar(kBarQnRaw), 1);
     mbar_init(bar(kBarQnFree), 1);
     mbar_init(bar(kBarQDone), 1);
     mbar_init(bar(kBarSFull), 1);
@@ -201,14 +241,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     // The whole warp walks the tiles; lane 0 issues the copies. Page ids are
     // fetched 32 at a time by the warp (one coalesced load) and handed out
-    // by shuffle, so a tile waits on no global load.
+    // by shuffle, so a tile waits on no global load. bf16 pools: tiles go
+    // straight into the ring. fp8 pools: tiles go into the fp8 ring and q
+    // into the ring unconverted; the converter warps finish both.
     const uint64_t kv_policy = l2_policy_evict_first();
     const int64_t layer_row0 = static_cast<int64_t>(a.layer) * a.num_pages * ps;
     const int oob_row = a.num_layers * a.num_pages * ps;  // reads as zeros
     const int rows_per_box = ps < kTile ? ps : kTile;
     const int boxes = kTile / rows_per_box;
-    uint32_t sl = 0;  // ring slot
-    int last_qn_item = -1;
+    const uint32_t row_bytes = kFp8 ? 256u + 32u : kWideChunks * 128u + 64u;
+    uint32_t sl = 0;     // ring slot
+    uint32_t ft = 0;     // fp8 ring slot
+    int last_qn_item = -1, last_q_item = -1, last_q_chunks = 0;
     uint32_t n_items = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
@@ -225,23 +269,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t stage = sl % kStages, use = sl / kStages;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarKvEmpty + stage), (use & 1u) ^ 1u, abort_flag));
         if (ok && lane == 0) {
-          const uint32_t fb = bar(kBarKvFull + stage);
+          const uint32_t fb = kFp8 ? bar(kBarRawQ + h) : bar(kBarKvFull + stage);
           mbar_arrive_expect_tx(fb, 2 * kQWideBytes);
           for (int c = 0; c < 2; ++c)
             tma_load_2d(sbase + kOffKV + stage * kStageBytes + c * kQWideBytes, &p.q_wide, fb,
                         wide_x + 64 * (2 * h + c), w.b * H);
+        }
+        if (ok) {
+          last_q_item = static_cast<int>(n_items);
+          last_q_chunks = h + 1;
         }
       }
       if (!ok) break;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQnFree), (n_items & 1u) ^ 1u, abort_flag));
       if (!ok) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kBarQnFull), kQNarrowBytes);
-        tma_load_2d(sbase + kOffQn, &p.q_narrow, bar(kBarQnFull), narrow_x, w.b * H);
+        const uint32_t qb = bar(kFp8 ? kBarQnRaw : kBarQnFull);
+        mbar_arrive_expect_tx(qb, kQNarrowBytes);
+        tma_load_2d(sbase + kOffQn, &p.q_narrow, qb, narrow_x, w.b * H);
       }
       last_qn_item = static_cast<int>(n_items);
-      for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++sl) {
-        const uint32_t stage = sl % kStages, use = sl / kStages;
+      for (int blk = w.blk_begin; blk < w.blk_end; ++blk) {
         int rows[4];
         int nbox = 0;
 #pragma unroll
@@ -272,20 +320,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           rows[bx] = row;
           ++nbox;
         }
+        // Every ring slot is waited for here, in order, for both pool types:
+        // a role that skipped slots could run two phases ahead of a slot's
+        // barrier, where a parity wait cannot tell the phases apart. For
+        // fp8 pools the converters write the slot after this tile's raw
+        // copy lands, which this wait precedes.
+        const uint32_t stage = sl % kStages, use = sl / kStages;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarKvEmpty + stage), (use & 1u) ^ 1u, abort_flag));
+        uint32_t full_bar, dst0;
+        if constexpr (kFp8) {
+          const uint32_t fs = ft % kF8Stages, fu = ft / kF8Stages;
+          ok = ok && __all_sync(0xffffffffu, mbar_wait(bar(kBarF8Empty + fs), (fu & 1u) ^ 1u, abort_flag));
+          full_bar = bar(kBarF8Full + fs);
+          dst0 = sbase + kOffF8 + fs * kF8Bytes;
+          ++ft;
+        } else {
+          full_bar = bar(kBarKvFull + stage);
+          dst0 = sbase + kOffKV + stage * kStageBytes;
+        }
+        ++sl;
         if (!ok) break;
         if (lane == 0) {
-          const uint32_t kvbar = bar(kBarKvFull + stage);
-          mbar_arrive_expect_tx(kvbar, static_cast<uint32_t>(nbox * rows_per_box * (kWideChunks * 128 + 64)));
-          const uint32_t dst0 = sbase + kOffKV + stage * kStageBytes;
+          mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(nbox * rows_per_box) * row_bytes);
 #pragma unroll
           for (int bx = 0; bx < 4; ++bx) {
             if (rows[bx] < 0) continue;
-            for (int c = 0; c < kWideChunks; ++c)
-              tma_load_2d_hint(dst0 + c * kWideBytes + bx * rows_per_box * 128, &p.kv_wide, kvbar,
-                               wide_x + 64 * c, rows[bx], kv_policy);
-            tma_load_2d_hint(dst0 + kWideChunks * kWideBytes + bx * rows_per_box * 64, &p.kv_narrow, kvbar,
-                             narrow_x, rows[bx], kv_policy);
+            if constexpr (kFp8) {
+              tma_load_2d_hint(dst0 + bx * rows_per_box * 256, &p.kv_wide, full_bar, wide_x, rows[bx], kv_policy);
+              tma_load_2d_hint(dst0 + kF8WideBytes + bx * rows_per_box * 32, &p.kv_narrow, full_bar, narrow_x,
+                               rows[bx], kv_policy);
+            } else {
+              for (int c = 0; c < kWideChunks; ++c)
+                tma_load_2d_hint(dst0 + c * kWideBytes + bx * rows_per_box * 128, &p.kv_wide, full_bar,
+                                 wide_x + 64 * c, rows[bx], kv_policy);
+              tma_load_2d_hint(dst0 + kWideChunks * kWideBytes + bx * rows_per_box * 64, &p.kv_narrow, full_bar,
+                               narrow_x, rows[bx], kv_policy);
+            }
           }
         }
       }
@@ -296,10 +366,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         flag_status(status, MLA_STATUS_TIMEOUT);
       }
       if (*abort_flag) {
-        // Let every copy already issued land before the CTA can exit.
-        for (uint32_t k = (sl > kStages ? sl - kStages : 0); k < sl; ++k)
-          mbar_wait(bar(kBarKvFull + k % kStages), (k / kStages) & 1u, nullptr);
-        if (last_qn_item >= 0) mbar_wait(bar(kBarQnFull), last_qn_item & 1, nullptr);
+        // Let every copy already issued land before the CTA can exit (bf16:
+        // ring slots complete KvFull; fp8: tiles complete F8Full and q
+        // chunks RawQ). Each of these waits is itself bounded.
+        if (kFp8) {
+          for (uint32_t k = (ft > kF8Stages ? ft - kF8Stages : 0); k < ft; ++k)
+            mbar_wait(bar(kBarF8Full + k % kF8Stages), (k / kF8Stages) & 1u, nullptr);
+          if (last_q_item >= 0)
+            for (int h = 0; h < last_q_chunks; ++h) mbar_wait(bar(kBarRawQ + h), last_q_item & 1, nullptr);
+        } else {
+          for (uint32_t k = (sl > kStages ? sl - kStages : 0); k < sl; ++k)
+            mbar_wait(bar(kBarKvFull + k % kStages), (k / kStages) & 1u, nullptr);
+        }
+        if (last_qn_item >= 0) mbar_wait(bar(kFp8 ? kBarQnRaw : kBarQnFull), last_qn_item & 1, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -309,7 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // S = q K^T with A read from TMEM (TS form), so shared memory streams
     // only the K tile through the tensor core.
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_bf16(128, kTile, false, false);
+      const uint32_t idesc_qk = kIdescQk;
       const uint32_t tQ = tmem + kColQ;
       const uint32_t tS = tmem + kColS;
       uint32_t sl = 0, g = 0, n_items = 0;
@@ -368,7 +447,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV issuer
     if (lane == 0) {
-      const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      const uint32_t idesc_pv = kIdescPv;
       const uint32_t tO = tmem + kColO;
       uint32_t sl = 0, g = 0;
       bool ok = true;
@@ -396,7 +475,87 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mma_commit(bar(kBarDrainPv));
       mbar_wait(bar(kBarDrainPv), 0, nullptr);
     }
-  } else if (warp != kPvWarp) {
+  } else if (kFp8 && warp >= kCvtWarp0) {
+    // ------------------------------------------------------------ converters (fp8 pools)
+    // Per item: q's bf16 chunks and rope part become f16 in place. Per tile:
+    // the raw e4m3 codes become f16 (exact: every e4m3 value is an f16) in
+    // the swizzled layout the tensor core reads, the one TMA writes for bf16
+    // pools. kv_scale is applied to the scores and the output instead.
+    const int ct = threadIdx.x - 32 * kCvtWarp0;  // 0..127
+    auto q_to_f16 = [&](uint32_t base, int units) {
+      for (int u = ct; u < units; u += 128) {
+        uint32_t x[4];
+        ld_shared_v4(base + u * 16, x[0], x[1], x[2], x[3]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[k] = pack_f16x2(__uint_as_float(x[k] << 16), __uint_as_float(x[k] & 0xffff0000u));
+        st_shared_v4(base + u * 16, x[0], x[1], x[2], x[3]);
+      }
+    };
+    uint32_t sl = 0, ft = 0, n_items = 0;
+    bool ok = true;
+    for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
+      const WorkItem w = items[it];
+      for (int h = 0; h < 2; ++h, ++sl) {
+        const uint32_t stage = sl % kStages;
+        if (!mbar_wait(bar(kBarRawQ + h), n_items & 1u, abort_flag)) { ok = false; break; }
+        q_to_f16(sbase + kOffKV + stage * kStageBytes, 2 * kQWideBytes / 16);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarKvFull + stage));
+      }
+      if (!ok) break;
+      if (!mbar_wait(bar(kBarQnRaw), n_items & 1u, abort_flag)) { ok = false; break; }
+      q_to_f16(sbase + kOffQn, kQNarrowBytes / 16);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(kBarQnFull));
+      for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++sl, ++ft) {
+        // The producer waited for this slot's release before the raw copy
+        // that completes F8Full was issued.
+        const uint32_t stage = sl % kStages;
+        const uint32_t fs = ft % kF8Stages, fu = ft / kF8Stages;
+        if (!mbar_wait(bar(kBarF8Full + fs), fu & 1u, abort_flag)) { ok = false; break; }
+        const uint32_t src = sbase + kOffF8 + fs * kF8Bytes;
+        const uint32_t dst = sbase + kOffKV + stage * kStageBytes;
+        // 16 codes per unit: 64 rows x 16 units of c_kv, then 64 rows x 2 of rope.
+        for (int u = ct; u < kTile * 18; u += 128) {
+          uint32_t x[4], y[8];
+          if (u < kTile * 16) {
+            const int r = u >> 4, c = u & 15;
+            ld_shared_v4(src + r * 256 + c * 16, x[0], x[1], x[2], x[3]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              y[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k] & 0xffffu));
+              y[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k] >> 16));
+            }
+            // dims 16c .. 16c+15: 128-byte-swizzled chunk c / 4, 16-byte pieces 2(c % 4) and +1
+            const uint32_t row_base = dst + (c >> 2) * kWideBytes + r * 128;
+            const int p0 = (c & 3) * 2;
+            st_shared_v4(row_base + ((p0 ^ (r & 7)) << 4), y[0], y[1], y[2], y[3]);
+            st_shared_v4(row_base + (((p0 + 1) ^ (r & 7)) << 4), y[4], y[5], y[6], y[7]);
+          } else {
+            const int v = u - kTile * 16, r = v >> 1, c = v & 1;
+            ld_shared_v4(src + kF8WideBytes + r * 32 + c * 16, x[0], x[1], x[2], x[3]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              y[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k] & 0xffffu));
+              y[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k] >> 16));
+            }
+            // rope dims 16c .. 16c+15: 64-byte-swizzled rows, pieces 2c and 2c+1
+            const uint32_t row_base = dst + kWideChunks * kWideBytes + r * 64;
+            const int sw = (r >> 1) & 3;
+            st_shared_v4(row_base + (((2 * c) ^ sw) << 4), y[0], y[1], y[2], y[3]);
+            st_shared_v4(row_base + (((2 * c + 1) ^ sw) << 4), y[4], y[5], y[6], y[7]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarF8Empty + fs));
+        mbar_arrive(bar(kBarKvFull + stage));
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      flag_status(status, MLA_STATUS_TIMEOUT);
+    }
+  } else if (warp < 2 + 8 && warp >= 2) {
     // ------------------------------------------------------------ exchange, softmax, correction, epilogue
     // Two warps per TMEM lane quarter q4 = w & 3 (rows / heads 32 q4 + lane,
     // one head per thread): warps 2-5 take tokens [0, 32) of every tile and
@@ -444,7 +603,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (nrow > 0) {
-        const float inv_l = valid ? 1.f / l : 0.f;
+        const float inv_l = valid ? a.out_scale / l : 0.f;  // out_scale: kv_scale for fp8 pools
 #pragma unroll 1
         for (int c = 0; c < 128 / 32; ++c) {
           uint32_t o[32];
@@ -514,10 +673,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       return true;
     };
+    // Fetching S(g+1) needs its ring slot, whose previous tile must have
+    // finished PV. Across an item boundary (two q slots in between) that
+    // tile is g itself unless the ring has at least 4 stages: there the
+    // first tile of the next item is fetched in its own iteration.
+    constexpr bool kEarlyAcrossItems = kStages >= 4;
     uint32_t g = 0, sl = 0, n_items = 0;
     bool ok = true;
     uint32_t xp[kHalf / 2];
-    if (total_tiles > 0) ok = fetch(0, xp);
+    bool have = false;  // xp holds this warp's partial of tile g
+    if (total_tiles > 0) {
+      ok = fetch(0, xp);
+      have = true;
+    }
     for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
       const WorkItem w = items[it];
       const int lo = max(w.blk_begin * kTile, w.tok_lo);
@@ -528,8 +696,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int base = blk * kTile + kHalf * half;  // first token of this warp
         const uint32_t b = g & 1u, u = g >> 1;
         const bool first_tile = blk == w.blk_begin;
+        if (!have && !fetch(g, xp)) { ok = false; break; }
         uint32_t xp_next[kHalf / 2];
-        if (static_cast<int>(g) + 1 < total_tiles && !fetch(g + 1, xp_next)) { ok = false; break; }
+        const bool have_next =
+            static_cast<int>(g) + 1 < total_tiles && (kEarlyAcrossItems || blk + 1 < w.blk_end);
+        if (have_next && !fetch(g + 1, xp_next)) { ok = false; break; }
         float alpha = 1.f;
         uint32_t pk[kHalf / 2];
         if (nrow > 0) {
@@ -582,7 +753,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const float p0 = fast_exp2(fmaf(s[2 * i], a.scale_log2, neg_m));
               const float p1 = fast_exp2(fmaf(s[2 * i + 1], a.scale_log2, neg_m));
               rs4[i & 3] += p0 + p1;
-              pk[i] = pack_bf16x2(p0, p1);
+              pk[i] = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             }
             l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
           } else {
@@ -592,6 +763,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < kHalf / 2; ++i) xp[i] = xp_next[i];
+        have = have_next;
         // Value rows of this tile outside [lo, hi) may hold anything (stale
         // or unwritten slots): zero this rank's value dims there so that
         // 0 * garbage cannot reach O. QK of the tile is complete here.
@@ -652,14 +824,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer may still address this CTA's shared memory
 }
 
-}  // namespace
-
-int decode_max_active_clusters() {
-  static int cached = -1;
-  if (cached > 0) return cached;
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
-  if (e != cudaSuccess) return -1;
+template <bool kFp8>
+int max_active_clusters_of() {
+  using C = Cfg<kFp8>;
+  if (cudaFuncSetAttribute(mla_decode_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+      cudaSuccess)
+    return -1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -670,22 +840,22 @@ int decode_max_active_clusters() {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cfg.gridDim = dim3(2 * (sms / 2));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel, &cfg);
-  if (e != cudaSuccess || n <= 0) return -1;
-  cached = n;
+  if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<kFp8>, &cfg) != cudaSuccess || n <= 0) return -1;
   return n;
 }
 
-cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& a, int clusters, cudaStream_t stream) {
+template <bool kFp8>
+cudaError_t launch_variant(const CUtensorMap* maps, const DecodeArgs& a, int clusters, cudaStream_t stream) {
+  using C = Cfg<kFp8>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -695,8 +865,26 @@ cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& a, int clus
   p.q_wide = maps[2];
   p.q_narrow = maps[3];
   p.a = a;
-  mla_decode_kernel<<<dim3(2 * clusters), dim3(kThreads), kSmemBytes, stream>>>(p);
+  mla_decode_kernel<kFp8><<<dim3(2 * clusters), dim3(C::kThreads), C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// Co-resident clusters: the smaller of the two variants' counts, so that one
+// plan serves either pool type.
+int decode_max_active_clusters() {
+  static int cached = -1;
+  if (cached > 0) return cached;
+  const int a = max_active_clusters_of<false>(), b = max_active_clusters_of<true>();
+  if (a <= 0 || b <= 0) return -1;
+  cached = a < b ? a : b;
+  return cached;
+}
+
+cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& a, int clusters, cudaStream_t stream) {
+  return a.dtype == MLA_DTYPE_FP8_E4M3 ? launch_variant<true>(maps, a, clusters, stream)
+                                       : launch_variant<false>(maps, a, clusters, stream);
 }
 
 }  // namespace mla

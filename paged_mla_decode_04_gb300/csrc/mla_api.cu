@@ -124,7 +124,6 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   if (!valid_pool(pool) || layer < 0 || layer >= pool->num_layers || batch < 0 || window < 0 || !workspace)
     return MLA_ERR_ARG;
   if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
-  if (pool->dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED;
   if (batch == 0) return MLA_OK;
   if (!q || !page_ids || !context_lens || !out || !aligned(q, 16) || !aligned(out, 16)) return MLA_ERR_ARG;
   if (!page_indptr && max_blocks <= 0) return MLA_ERR_ARG;
@@ -136,15 +135,25 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   const int ps = pool->page_size;
   const uint64_t total_rows = static_cast<uint64_t>(pool->num_layers) * pool->num_pages * ps;
   if (total_rows >= (1ull << 31)) return MLA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
-  // Each rank of the decode cluster reads 256 c_kv dims as 64-dim boxes
-  // (128-byte swizzle) and 32 rope dims as one 32-dim box (64-byte swizzle).
+  // Each rank of the decode cluster reads its 256 c_kv dims and 32 rope
+  // dims of every row: bf16 pools as 64-dim boxes (128-byte swizzle) and one
+  // 32-dim box (64-byte swizzle), the layout the tensor core reads; fp8
+  // pools as one 256-byte and one 32-byte box, unswizzled, which the kernel
+  // widens to f16 in that same layout.
   CUtensorMap maps[4];
   const uint32_t box_rows = ps < mla::kBlockTokens ? ps : mla::kBlockTokens;
   const uint64_t q_rows = static_cast<uint64_t>(batch) * num_heads;
-  if (!make_map_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->data, total_rows, mla::kDimRow,
-                   mla::kDimRow * 2, 64, box_rows) ||
-      !make_map_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->data, total_rows, mla::kDimRow,
-                   mla::kDimRow * 2, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  const bool fp8 = pool->dtype == MLA_DTYPE_FP8_E4M3;
+  const bool kv_ok =
+      fp8 ? make_map_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, pool->data, total_rows, mla::kDimRow, mla::kDimRow,
+                        256, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                make_map_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, pool->data, total_rows, mla::kDimRow,
+                            mla::kDimRow, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE)
+          : make_map_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->data, total_rows, mla::kDimRow,
+                        mla::kDimRow * 2, 64, box_rows) &&
+                make_map_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pool->data, total_rows, mla::kDimRow,
+                            mla::kDimRow * 2, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!kv_ok ||
       !make_map_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, q_rows, mla::kDimRow, mla::kDimRow * 2, 64,
                    128) ||
       !make_map_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, q_rows, mla::kDimRow, mla::kDimRow * 2, 32,
@@ -171,7 +180,10 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   a.layer = layer;
   a.dtype = pool->dtype;
   a.kv_scale = pool->kv_scale;
-  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  // fp8 pools: scores and output are scaled by kv_scale instead of the
+  // codes (the kernel computes on the exact codes).
+  a.scale_log2 = softmax_scale * 1.4426950408889634f * (fp8 ? pool->kv_scale : 1.f);
+  a.out_scale = fp8 ? pool->kv_scale : 1.f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = mla::launch_decode(maps, a, cmax, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;

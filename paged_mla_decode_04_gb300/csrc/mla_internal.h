@@ -97,7 +97,8 @@ struct DecodeArgs {
   int layer;
   int dtype;
   float kv_scale;
-  float scale_log2;  // softmax_scale * log2(e)
+  float scale_log2;  // softmax_scale * log2(e) (* kv_scale for fp8 pools)
+  float out_scale;   // 1, or kv_scale for fp8 pools (codes are dequantised by scaling O)
 };
 
 // kv_write.cu
