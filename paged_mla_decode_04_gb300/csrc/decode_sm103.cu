@@ -34,10 +34,11 @@
 // TMEM columns: O [0, 256) fp32, q [256, 400), S [400, 464) fp32, P [464,
 // 496) bf16 pairs; S and P are single-buffered (the next QK waits for S to be
 // read, the next P for the previous PV).
-// Warp roles per CTA (352 threads): warp 0 TMA producer, warp 1 TMEM owner
-// and QK issuer, warps 2-9 exchange / softmax / correction / epilogue (warp
-// w works on TMEM lane quarter w & 3, one head per thread, warps 2-5 on the
-// first 32 tokens of a tile and 6-9 on the last 32), warp 10 PV issuer.
+// Warp roles per CTA (352 threads; 480 for fp8 pools): warp 0 TMA producer,
+// warp 1 TMEM owner and QK issuer, warps 2-9 exchange / softmax / correction
+// / epilogue (warp w works on 16 lanes of TMEM lane quarter w & 3; a head's
+// row belongs to two threads, tokens [0, 32) and [32, 64) of each tile),
+// warp 10 PV issuer, warps 11-14 (fp8 pools) widen fp8 tiles to f16.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -74,9 +75,7 @@ struct Cfg {
   static constexpr int kOffKV = kOffQn + kQNarrowBytes;
   static constexpr int kOffF8 = kOffKV + kStages * kStageBytes;
   static constexpr int kOffX = kOffF8 + (kFp8 ? kF8Stages * kF8Bytes : 0);  // [2 buffers]
-  static constexpr int kOffRed = kOffX + 2 * kXBytes;  // [2 tile parities][4 quarters][2 halves][32] fp32
-  static constexpr int kOffLRed = kOffRed + 2048;      // [4 quarters][2 halves][32] fp32
-  static constexpr int kOffBar = kOffLRed + 1024;
+  static constexpr int kOffBar = kOffX + 2 * kXBytes;
   static constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // barriers + alignment slack
   static constexpr int kThreads = kFp8 ? 480 : 352;
   static_assert(kOffKV % 1024 == 0 && kOffF8 % 1024 == 0 && kOffX % 1024 == 0, "alignment");
@@ -107,9 +106,7 @@ enum Bar {
   kBarSFree,
   kBarXFull,                       // [2 buffers][4 quarters][2 halves]: the peer's partial rows landed
   kBarXFree = kBarXFull + 16,      // [2 buffers][4 quarters][2 halves]: the peer read this rank's partial rows
-  kBarPairMax = kBarXFree + 16,    // [4 quarters]: both halves' row maxima of the tile posted
-  kBarPairSum = kBarPairMax + 4,   // [4 quarters]: both halves' row sums of the item posted
-  kBarOFixed = kBarPairSum + 4,    // P in TMEM and O rescaled for this tile
+  kBarOFixed = kBarXFree + 16,     // P in TMEM and O rescaled for this tile
   kBarPvDone,                      // PV of the tile done
   kBarDrain,
   kBarDrainPv,
@@ -148,8 +145,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   constexpr int kOffKV = C::kOffKV;
   constexpr int kOffF8 = C::kOffF8;
   constexpr int kOffX = C::kOffX;
-  constexpr int kOffRed = C::kOffRed;
-  constexpr int kOffLRed = C::kOffLRed;
   constexpr int kOffBar = C::kOffBar;
   // fp8 pools run the tensor core on f16 (q and P converted, codes exact).
   constexpr uint32_t kIdescQk = kFp8 ? idesc_f16(128, kTile, false, false) : idesc_bf16(128, kTile, false, false);
@@ -204,10 +199,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarSFree), 256);
     mbar_init(bar(kBarOFixed), 256);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(bar(kBarPairMax + i), 64);
-      mbar_init(bar(kBarPairSum + i), 64);
-    }
     mbar_init(bar(kBarPvDone), 1);
     for (int i = 0; i < 16; ++i) {
       mbar_init(bar(kBarXFull + i), 1);
@@ -423,16 +414,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           if (!mbar_wait(bar(kBarSFree), (g & 1u) ^ 1u, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t kv = sbase + kOffKV + stage * kStageBytes;
+          // Descriptors of the tile's first chunk; the others differ only in
+          // the start address field (bytes / 16).
+          const uint64_t dw = sdesc_sw128(kv, 16, 1024);
+          const uint64_t dn = sdesc_sw64(kv + kWideChunks * kWideBytes, 512);
 #pragma unroll
           for (int c = 0; c < kWideChunks; ++c)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_bf16_ts(tS, tQ + 8u * (4 * c + k), sdesc_sw128(kv + c * kWideBytes + k * 32, 16, 1024), idesc_qk,
-                          (c | k) != 0);
+              mma_bf16_ts(tS, tQ + 8u * (4 * c + k), dw + static_cast<uint64_t>((c * kWideBytes + k * 32) >> 4),
+                          idesc_qk, (c | k) != 0);
 #pragma unroll
           for (int k = 0; k < 2; ++k)
-            mma_bf16_ts(tS, tQ + 128u + 8u * k, sdesc_sw64(kv + kWideChunks * kWideBytes + k * 32, 512), idesc_qk,
-                        1u);
+            mma_bf16_ts(tS, tQ + 128u + 8u * k, dn + static_cast<uint64_t>((k * 32) >> 4), idesc_qk, 1u);
           mma_commit(bar(kBarSFull));
         }
         if (ok) mma_commit(bar(kBarQDone));  // every QK of this item complete: q may be replaced
@@ -459,10 +453,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           if (!mbar_wait(bar(kBarOFixed), g & 1u, abort_flag)) { ok = false; break; }
           tc_fence_after();
           fence_proxy_async_smem();
-          const uint32_t v0 = sbase + kOffKV + (sl % kStages) * kStageBytes;
+          const uint64_t dv = sdesc_sw128(sbase + kOffKV + (sl % kStages) * kStageBytes, kWideBytes, 1024);
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ts(tO, tmem + kColP + 8u * k, sdesc_sw128(v0 + k * 16 * 128, kWideBytes, 1024), idesc_pv,
+            mma_bf16_ts(tO, tmem + kColP + 8u * k, dv + static_cast<uint64_t>((k * 16 * 128) >> 4), idesc_pv,
                         (t | k) != 0);
           mma_commit(bar(kBarKvEmpty + sl % kStages));
           mma_commit(bar(kBarPvDone));
@@ -557,23 +551,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     }
   } else if (warp < 2 + 8 && warp >= 2) {
     // ------------------------------------------------------------ exchange, softmax, correction, epilogue
-    // Two warps per TMEM lane quarter q4 = w & 3 (rows / heads 32 q4 + lane,
-    // one head per thread): warps 2-5 take tokens [0, 32) of every tile and
-    // warps 6-9 tokens [32, 64), so each SM sub-partition runs two of them
-    // and hides one's latencies behind the other. Per tile g: this rank's
-    // partial scores, rounded to bf16, go to the peer (st.async) and the
-    // peer's arrive the same way; both ranks then form the same sum
-    // bf16(S_0) + bf16(S_1) (fp32 addition commutes), the two halves of a
-    // row agree on its running max through shared memory, and both ranks
-    // run the same online softmax and keep the same P in their own TMEM.
+    // Warp w works on 16 rows (heads) of TMEM lane quarter q4 = w & 3: warps
+    // 2-5 on its lanes 0-15, warps 6-9 on lanes 16-31. A row belongs to two
+    // threads: t and t + 16 hold its tokens [0, 32) and [32, 64) of every
+    // tile (and value dims [0, 128) and [128, 256) of this rank's O), so the
+    // row max and sum need one shuffle and no other warp. Per tile g: this
+    // rank's partial scores, rounded to bf16, go to the peer (st.async) and
+    // the peer's arrive the same way; both ranks form the same sum
+    // bf16(S_0) + bf16(S_1) (fp32 addition commutes), run the same online
+    // softmax and keep the same P in their own TMEM.
     const int q4 = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int nrow = min(max(H - 32 * q4, 0), 32);  // valid heads in this quarter
-    const int row = 32 * q4 + lane;                 // head of this lane
-    const bool valid = lane < nrow;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-    const uint32_t tO = tmem + lane_base + kColO + 128u * half;  // this warp's half of O
-    const uint32_t dim0 = 256u * rank + 128u * half;
+    const int half = (warp - 2) >> 2;               // lane half of the quarter
+    const int th = lane >> 4;                       // token half of a tile / value-dim half
+    const int row = 32 * q4 + 16 * half + (lane & 15);
+    const int nrow = min(max(H - 32 * q4 - 16 * half, 0), 16);  // valid heads of this warp
+    const bool valid = (lane & 15) < nrow;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q4 + 16 * half) << 16;
+    const uint32_t tO = tmem + lane_base + kColO;   // this warp's 16 rows of O
+    const uint32_t dim0 = 256u * rank + 128u * th;  // first value dim of this thread
     constexpr int kHalf = kTile / 2;
     auto wwait = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(b, parity, abort_flag));
@@ -581,20 +576,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     auto wwait_cluster = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait<true>(b, parity, abort_flag));
     };
-    // X[b]: the peer's partial rows; per quarter and half 32 rows of 32
-    // tokens as 16-byte pieces, piece-major (lane-contiguous).
-    auto xq = [&](uint32_t b) { return sbase + kOffX + b * kXBytes + q4 * (32 * kTile * 2) + half * (32 * kHalf * 2); };
+    // X[b]: the peer's partial rows; per warp 16 rows x 64 tokens as 16-byte
+    // pieces, piece-major (lane-contiguous): piece j of thread t holds
+    // tokens 32 th + 8 j .. + 8 of row t & 15.
+    auto xq = [&](uint32_t b) { return sbase + kOffX + b * kXBytes + q4 * (32 * kTile * 2) + half * (16 * kTile * 2); };
     auto xfull = [&](uint32_t b) { return bar(kBarXFull + 8 * b + 2 * q4 + half); };
     auto xfree = [&](uint32_t b) { return bar(kBarXFree + 8 * b + 2 * q4 + half); };
-    // Row maxima / row sums handed between the two warps of a quarter.
-    auto red = [&](uint32_t par, int h) { return sbase + kOffRed + par * 1024 + q4 * 256 + h * 128 + lane * 4; };
-    auto lred = [&](int h) { return sbase + kOffLRed + q4 * 256 + h * 128 + lane * 4; };
-    // Epilogue of an item: wait for its last PV, normalise this warp's 128
-    // value dims, store.
+    // The peer's copies of this warp's exchange buffers and barriers.
+    const uint32_t peer_xq0 = mapa(xq(0), peer), peer_xq1 = mapa(xq(1), peer);
+    const uint32_t peer_xfull0 = mapa(xfull(0), peer), peer_xfull1 = mapa(xfull(1), peer);
+    const uint32_t peer_xfree0 = mapa(xfree(0), peer), peer_xfree1 = mapa(xfree(1), peer);
+    // Epilogue of an item: wait for its last PV, normalise this thread's
+    // 128 value dims, store.
     auto store_item = [&](const WorkItem& w, uint32_t g_last, float m, float l) -> bool {
       if (!wwait(bar(kBarPvDone), g_last & 1u)) return false;
       tc_fence_after();
-      if (rank == 0 && half == 0 && valid) {
+      if (rank == 0 && th == 0 && valid) {
         const float lse2 = m + log2f(l);
         if (w.slot < 0) {
           if (a.lse) a.lse[static_cast<size_t>(w.b) * H + row] = lse2 * 0.69314718055994531f;
@@ -605,17 +602,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       if (nrow > 0) {
         const float inv_l = valid ? a.out_scale / l : 0.f;  // out_scale: kv_scale for fp8 pools
 #pragma unroll 1
-        for (int c = 0; c < 128 / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld16(tO + c * 32, o);
-          tmem_ld16(tO + c * 32 + 16, o + 16);
+        for (int c = 0; c < 128 / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld_h16<128>(tO + c * 16, o);
           tmem_wait_ld();
           if (valid) {
             if (w.slot < 0) {
               __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                                   (static_cast<size_t>(w.b) * H + row) * kDimCkv + dim0 + c * 32;
+                                   (static_cast<size_t>(w.b) * H + row) * kDimCkv + dim0 + c * 16;
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
+              for (int v = 0; v < 2; ++v) {
                 uint4 ov;
                 ov.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
                 ov.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
@@ -625,9 +621,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
               }
             } else {
               float* dst = reinterpret_cast<float*>(ws + a.lay.partial_o) +
-                           (static_cast<size_t>(w.slot) * H + row) * kDimCkv + dim0 + c * 32;
+                           (static_cast<size_t>(w.slot) * H + row) * kDimCkv + dim0 + c * 16;
 #pragma unroll
-              for (int v = 0; v < 8; ++v)
+              for (int v = 0; v < 4; ++v)
                 reinterpret_cast<float4*>(dst)[v] =
                     make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
@@ -643,7 +639,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     // overlaps the exponentials instead of sitting in this loop.
     int total_tiles = 0;
     for (int it = it_begin; it < it_end; ++it) total_tiles += items[it].blk_end - items[it].blk_begin;
-    // Wait for S(gg), keep this rank's partial (this warp's 32 tokens) as
+    // Wait for S(gg), keep this rank's partial (this thread's 32 tokens) as
     // bf16 pairs in xp, release S, and send the pairs to the peer once it
     // has read that buffer's previous contents.
     auto fetch = [&](uint32_t gg, uint32_t* xp) -> bool {
@@ -652,8 +648,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       tc_fence_after();
       if (nrow > 0) {
         uint32_t r[kHalf];
-        tmem_ld16(tmem + lane_base + kColS + kHalf * half, r);
-        tmem_ld16(tmem + lane_base + kColS + kHalf * half + 16, r + 16);
+        tmem_ld_h16<kHalf>(tmem + lane_base + kColS, r);
+        tmem_ld_h16<kHalf>(tmem + lane_base + kColS + 16, r + 16);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < kHalf / 2; ++i) xp[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
@@ -663,13 +659,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       if (nrow > 0) {
         if (!wwait(xfree(b), (u & 1u) ^ 1u)) return false;
         if (valid) {
-          const uint32_t dst = mapa(xq(b), peer);
-          const uint32_t fb = mapa(xfull(b), peer);
+          const uint32_t dst = b ? peer_xq1 : peer_xq0;
+          const uint32_t fb = b ? peer_xfull1 : peer_xfull0;
 #pragma unroll
           for (int j = 0; j < kHalf / 8; ++j)
             st_async_v4(dst + (j * 32 + lane) * 16, xp[4 * j], xp[4 * j + 1], xp[4 * j + 2], xp[4 * j + 3], fb);
         }
-        if (lane == 0) mbar_arrive_expect_tx(xfull(b), static_cast<uint32_t>(nrow * kHalf * 2));
+        if (lane == 0) mbar_arrive_expect_tx(xfull(b), static_cast<uint32_t>(2 * nrow * kHalf * 2));
       }
       return true;
     };
@@ -678,22 +674,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     // tile is g itself unless the ring has at least 4 stages: there the
     // first tile of the next item is fetched in its own iteration.
     constexpr bool kEarlyAcrossItems = kStages >= 4;
-    uint32_t g = 0, sl = 0, n_items = 0;
+    uint32_t g = 0, sl = 0;
     bool ok = true;
     uint32_t xp[kHalf / 2];
-    bool have = false;  // xp holds this warp's partial of tile g
+    bool have = false;  // xp holds this thread's partial of tile g
     if (total_tiles > 0) {
       ok = fetch(0, xp);
       have = true;
     }
-    for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
+    for (int it = it_begin; it < it_end && ok; ++it) {
       const WorkItem w = items[it];
       const int lo = max(w.blk_begin * kTile, w.tok_lo);
       const int hi = min(w.blk_end * kTile, w.tok_hi);
-      float m = -CUDART_INF_F, l = 0.f;  // l: this warp's tokens only
+      float m = -CUDART_INF_F, l = 0.f;  // l: this thread's tokens only
       sl += 2;  // the item's q slots
       for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++g, ++sl) {
-        const int base = blk * kTile + kHalf * half;  // first token of this warp
+        const int base = blk * kTile + kHalf * th;  // first token of this thread
         const uint32_t b = g & 1u, u = g >> 1;
         const bool first_tile = blk == w.blk_begin;
         if (!have && !fetch(g, xp)) { ok = false; break; }
@@ -705,7 +701,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         uint32_t pk[kHalf / 2];
         if (nrow > 0) {
           if (!wwait_cluster(xfull(b), u & 1u)) { ok = false; break; }
-          float s[kHalf];
+          // Scores as packed fp32 pairs (tokens 2i, 2i+1): both ranks add the
+          // same two bf16 partials.
+          uint64_t s2[kHalf / 2];
           float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
           if (valid) {
 #pragma unroll
@@ -713,49 +711,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
               uint32_t x[4];
               ld_shared_v4(xq(b) + (j * 32 + lane) * 16, x[0], x[1], x[2], x[3]);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int e = 8 * j + 2 * k;
-                s[e] = __uint_as_float(xp[4 * j + k] << 16) + __uint_as_float(x[k] << 16);
-                s[e + 1] = __uint_as_float(xp[4 * j + k] & 0xffff0000u) + __uint_as_float(x[k] & 0xffff0000u);
-              }
+              for (int k = 0; k < 4; ++k) s2[4 * j + k] = f2_add(f2_from_bf16x2(xp[4 * j + k]), f2_from_bf16x2(x[k]));
             }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive_remote_relaxed(mapa(xfree(b), peer));  // X[b] read
+          if (lane == 0) mbar_arrive_remote_relaxed(b ? peer_xfree1 : peer_xfree0);  // X[b] read
           if (valid) {
             if (lo > base || hi < base + kHalf) {
 #pragma unroll
-              for (int i = 0; i < kHalf; ++i) {
-                const int pos = base + i;
-                if (pos < lo || pos >= hi) s[i] = -CUDART_INF_F;
+              for (int i = 0; i < kHalf / 2; ++i) {
+                float s0, s1;
+                f2_split(s2[i], s0, s1);
+                const int pos = base + 2 * i;
+                if (pos < lo || pos >= hi) s0 = -CUDART_INF_F;
+                if (pos + 1 < lo || pos + 1 >= hi) s1 = -CUDART_INF_F;
+                s2[i] = f2_make(s0, s1);
               }
             }
 #pragma unroll
-            for (int i = 0; i < kHalf; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+            for (int i = 0; i < kHalf / 2; ++i) {
+              float s0, s1;
+              f2_split(s2[i], s0, s1);
+              mx4[(2 * i) & 3] = fmaxf(mx4[(2 * i) & 3], s0);
+              mx4[(2 * i + 1) & 3] = fmaxf(mx4[(2 * i + 1) & 3], s1);
+            }
           }
-          // The row max over both halves (scores are scaled by a positive
-          // factor, so the max of the raw sums is taken).
-          const float mx_half = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-          st_shared_f32(red(g & 1u, half), mx_half);
-          mbar_arrive(bar(kBarPairMax + q4));
-          if (!wwait(bar(kBarPairMax + q4), g & 1u)) { ok = false; break; }
+          // The row max over both token halves (scores are scaled by a
+          // positive factor, so the max of the raw sums is taken).
+          float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * a.scale_log2;
           if (valid) {
-            const float mx = fmaxf(mx_half, ld_shared_f32(red(g & 1u, half ^ 1))) * a.scale_log2;
             if (mx > m + kRescaleThreshold) {
               alpha = fast_exp2(m - mx);  // 0 on the first tile (m = -inf)
               l *= alpha;
               m = mx;
             }
-            const float neg_m = -m;
-            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t c2 = f2_make(a.scale_log2, a.scale_log2);
+            const uint64_t nm2 = f2_make(-m, -m);
+            uint64_t rs2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) {
-              const float p0 = fast_exp2(fmaf(s[2 * i], a.scale_log2, neg_m));
-              const float p1 = fast_exp2(fmaf(s[2 * i + 1], a.scale_log2, neg_m));
-              rs4[i & 3] += p0 + p1;
+              float t0, t1;
+              f2_split(f2_fma(s2[i], c2, nm2), t0, t1);
+              const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+              rs2[i & 1] = f2_add(rs2[i & 1], f2_make(p0, p1));
               pk[i] = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             }
-            l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+            float r0, r1, r2, r3;
+            f2_split(rs2[0], r0, r1);
+            f2_split(rs2[1], r2, r3);
+            l += (r0 + r1) + (r2 + r3);
           } else {
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) pk[i] = 0;
@@ -770,7 +775,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         const int tbase = blk * kTile;
         if (lo > tbase || hi < tbase + kTile) {
           const uint32_t v0 = sbase + kOffKV + (sl % kStages) * kStageBytes;
-          for (int e = 32 * q4 + 128 * half + lane; e < kTile * kWideChunks * 8; e += 256) {
+          for (int e = threadIdx.x - 64; e < kTile * kWideChunks * 8; e += 256) {
             const int rr = e >> 5, c = (e >> 3) & 3, piece = e & 7;
             const int pos = tbase + rr;
             if (pos < lo || pos >= hi) st_shared_v4(v0 + c * kWideBytes + rr * 128 + piece * 16, 0, 0, 0, 0);
@@ -782,18 +787,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         if (!wwait(bar(kBarPvDone), (g & 1u) ^ 1u)) { ok = false; break; }
         tc_fence_after();
         if (nrow > 0) {
-          tmem_st16(tmem + lane_base + kColP + (kHalf / 2) * half, pk);
-          // Rescale this warp's half of the quarter's O rows before PV(g)
-          // when the max moved (both halves see the same alpha).
+          tmem_st_h16<kHalf / 2>(tmem + lane_base + kColP, pk);
+          // Rescale this thread's half of the row's O before PV(g) when the
+          // max moved (both threads of a row see the same alpha).
           if (!first_tile && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
 #pragma unroll 1
             for (int c = 0; c < 128 / 16; ++c) {
               uint32_t o[16];
-              tmem_ld16(tO + c * 16, o);
+              tmem_ld_h16<128>(tO + c * 16, o);
               tmem_wait_ld();
 #pragma unroll
               for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st16(tO + c * 16, o);
+              tmem_st_h16<128>(tO + c * 16, o);
             }
           }
           tmem_wait_st();
@@ -802,13 +807,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         mbar_arrive(bar(kBarOFixed));
       }
       if (!ok) break;
-      // The row sum over both halves.
-      if (nrow > 0) {
-        st_shared_f32(lred(half), l);
-        mbar_arrive(bar(kBarPairSum + q4));
-        if (!wwait(bar(kBarPairSum + q4), n_items & 1u)) { ok = false; break; }
-        l += ld_shared_f32(lred(half ^ 1));
-      }
+      // The row sum over both token halves.
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
       if (!store_item(w, g - 1, m, l)) { ok = false; break; }
     }
     if (!ok) {
