@@ -139,8 +139,9 @@ int mla_decode_plan(const int32_t* context_lens, int batch, int num_heads,
  * read (the bounded-prefix rule of SGLang PR #32972, Correction); a page id
  * outside [0, num_pages) sets MLA_STATUS_BAD_PAGE and its rows read as zero.
  *   q:   device, [batch][num_heads][576] bf16 (absorbed nope 512 || rope 64).
- *   out: device, [batch][num_heads][512] bf16. lse: device [batch][num_heads]
- *        fp32 or NULL.
+ *   out: device, [batch][num_heads][512] bf16, 32-byte aligned (the kernel
+ *        writes whole 32-byte sectors). lse: device [batch][num_heads] fp32
+ *        or NULL. q must be 16-byte aligned; MLA_ERR_ARG otherwise.
  *   workspace: the one last given to mla_decode_plan with the same batch,
  *        num_heads, page_size and window.
  * num_heads must be 16, 32, 64 or 128 (MLA_ERR_UNSUPPORTED otherwise). The

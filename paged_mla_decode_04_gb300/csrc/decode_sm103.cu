@@ -607,26 +607,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           tmem_ld_h16<128>(tO + c * 16, o);
           tmem_wait_ld();
           if (valid) {
+            // Whole 32-byte sectors per store (16 bf16 or 8 fp32 dims).
             if (w.slot < 0) {
               __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
                                    (static_cast<size_t>(w.b) * H + row) * kDimCkv + dim0 + c * 16;
+              uint32_t pk[8];
 #pragma unroll
-              for (int v = 0; v < 2; ++v) {
-                uint4 ov;
-                ov.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-                ov.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-                ov.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-                ov.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-                reinterpret_cast<uint4*>(dst)[v] = ov;
-              }
+              for (int i = 0; i < 8; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+              st_global_v8(dst, pk);
             } else {
               float* dst = reinterpret_cast<float*>(ws + a.lay.partial_o) +
                            (static_cast<size_t>(w.slot) * H + row) * kDimCkv + dim0 + c * 16;
 #pragma unroll
-              for (int v = 0; v < 4; ++v)
-                reinterpret_cast<float4*>(dst)[v] =
-                    make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv_l);
+              st_global_v8(dst, o);
+              st_global_v8(dst + 8, o + 8);
             }
           }
         }

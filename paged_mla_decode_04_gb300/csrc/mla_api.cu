@@ -125,7 +125,7 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
     return MLA_ERR_ARG;
   if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
   if (batch == 0) return MLA_OK;
-  if (!q || !page_ids || !context_lens || !out || !aligned(q, 16) || !aligned(out, 16)) return MLA_ERR_ARG;
+  if (!q || !page_ids || !context_lens || !out || !aligned(q, 16) || !aligned(out, 32)) return MLA_ERR_ARG;
   if (!page_indptr && max_blocks <= 0) return MLA_ERR_ARG;
   if (!(softmax_scale > 0.f)) return MLA_ERR_ARG;
   const int cmax = max_clusters();
