@@ -20,11 +20,17 @@ namespace mla {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+// A work item costs about this many 64-token blocks beyond its blocks (its
+// epilogue and the pipeline refill when the next item starts): small batches
+// count it in the balance, so clusters that start more requests get fewer
+// blocks.
+constexpr int kItemCostBlocks = 2;
 
 // Block-wide exclusive scan of one int per thread; returns the prefix and
 // writes the block total to *total.
 __device__ int block_excl_scan(int v, int* total, int* smem32) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
   int x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -34,7 +40,7 @@ __device__ int block_excl_scan(int v, int* total, int* smem32) {
   if (lane == 31) smem32[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = smem32[lane];
+    int w = lane < nwarps ? smem32[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, w, o);
@@ -49,12 +55,18 @@ __device__ int block_excl_scan(int v, int* total, int* smem32) {
   return warp_prefix + x - v;
 }
 
+// The products below stay under 2^32 whenever T * C does (T blocks, C <= 1024
+// clusters), which is then divided in 32 bits; 64-bit division is a long
+// software routine.
 __device__ __forceinline__ long long range_lo(long long c, long long T, long long C) {
+  if (T * C < (1ll << 32)) return static_cast<unsigned>(c * T) / static_cast<unsigned>(C);
   return c * T / C;
 }
 
 // Cluster whose range [lo(c), lo(c+1)) holds block x (requires T >= C).
 __device__ __forceinline__ int cluster_of(long long x, long long T, long long C) {
+  if (T * C + T < (1ll << 32))
+    return static_cast<int>((static_cast<unsigned>((x + 1) * C + T - 1)) / static_cast<unsigned>(T)) - 1;
   return static_cast<int>(((x + 1) * C + T - 1) / T - 1);
 }
 
@@ -72,7 +84,89 @@ __global__ void __launch_bounds__(kPlanThreads)
   if (tid == 0) bad_len = 0;
   __syncthreads();
 
-  // Pass 1: blocks per request and their offsets in the concatenated order.
+  if (B <= static_cast<int>(blockDim.x)) {
+    // One request per thread, everything in registers: no pass through
+    // global memory between the scans. Request b weighs its n_b blocks plus
+    // kItemCostBlocks; the weights are concatenated in request order and cut
+    // into C equal ranges; a request's blocks sit after its extra weight.
+    __shared__ int last_cluster[kPlanThreads];
+    int L = 0, s = 0, first = 0, n = 0;
+    if (tid < B) {
+      L = lens[tid];
+      if (L < 0) {
+        bad_len = 1;
+        L = 0;
+      }
+      s = window > 0 ? max(0, L + 1 - window) : 0;
+      first = s / kBlockTokens;
+      n = L / kBlockTokens - first + 1;
+    }
+    int T32;
+    const int off = block_excl_scan(tid < B ? n + kItemCostBlocks : 0, &T32, smem32) + kItemCostBlocks;
+    const long long T = T32;
+    const long long C = T > 0 ? (T < C_req ? T : C_req) : 1;
+    int cf = 0, cl = -1, ns = 0;
+    if (tid < B) {
+      cf = cluster_of(off, T, C);
+      cl = cluster_of(static_cast<long long>(off) + n - 1, T, C);
+      ns = cl - cf + 1;
+    }
+    last_cluster[tid] = cl;
+    int t_items, t_part, t_split;
+    const int item0 = block_excl_scan(ns, &t_items, smem32);
+    const int part0 = block_excl_scan(ns > 1 ? ns : 0, &t_part, smem32);
+    const int split0 = block_excl_scan(ns > 1 ? 1 : 0, &t_split, smem32);
+    if (tid < B) {
+      for (int k = 0; k < ns; ++k) {
+        const int c = cf + k;
+        const long long lo = max(static_cast<long long>(off), range_lo(c, T, C));
+        const long long hi = min(static_cast<long long>(off) + n, range_lo(c + 1, T, C));
+        WorkItem w;
+        w.b = tid;
+        w.blk_begin = first + static_cast<int>(lo - off);
+        w.blk_end = first + static_cast<int>(hi - off);
+        w.slot = ns > 1 ? part0 + k : -1;
+        w.tok_lo = s;
+        w.tok_hi = L + 1;
+        w.cluster = c;
+        w.pad = 0;
+        items[item0 + k] = w;
+      }
+      if (ns > 1) {
+        SplitRequest r;
+        r.b = tid;
+        r.num_splits = ns;
+        r.first_partial = part0;
+        r.pad = 0;
+        split[split0] = r;
+      }
+      // First item of each cluster after the previous request's last one
+      // (clusters whose range holds no block of any request get an empty
+      // range at this request's first item).
+      const int prev = tid > 0 ? last_cluster[tid - 1] : -1;
+      for (int c = prev + 1; c <= cl; ++c) cstart[c] = item0 + (c > cf ? c - cf : 0);
+    }
+    const int cl_last = B > 0 ? last_cluster[B - 1] : -1;
+    for (int c = cl_last + 1 + tid; c <= C_req; c += blockDim.x) cstart[c] = t_items;
+    __syncthreads();
+    if (tid == 0) {
+      if (bad_len) atomicOr(&hd->status, MLA_STATUS_BAD_LENGTH);
+      hd->batch = B;
+      hd->num_heads = H;
+      hd->page_size = ps;
+      hd->window = window;
+      hd->num_clusters = static_cast<int>(C);
+      hd->total_blocks = static_cast<int>(T);
+      hd->num_items = t_items;
+      hd->num_partials = t_part;
+      hd->num_split = t_split;
+      hd->planned = 1;
+    }
+    return;
+  }
+
+  // Larger batches: pass 1, blocks per request and their offsets in the
+  // concatenated order.
   long long T = 0;
   for (int base = 0; base < B; base += kPlanThreads) {
     const int i = base + tid;
@@ -232,8 +326,11 @@ __global__ void __launch_bounds__(32 * kMergeHeadsPerBlock)
 cudaError_t launch_plan(const int32_t* context_lens, int batch, int heads, int page_size,
                         int window, int clusters, uint8_t* ws, const WsLayout& lay,
                         cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(context_lens, batch, heads, page_size, window,
-                                              clusters, ws, lay);
+  // Small batches: one thread per request (whole warps), every step in
+  // registers; larger ones: 1024 threads looping over the batch.
+  const int threads = batch <= kPlanThreads ? ((batch + 31) / 32 * 32 > 32 ? (batch + 31) / 32 * 32 : 32)
+                                            : kPlanThreads;
+  plan_kernel<<<1, threads, 0, stream>>>(context_lens, batch, heads, page_size, window, clusters, ws, lay);
   return cudaGetLastError();
 }
 
