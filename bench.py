@@ -33,7 +33,7 @@ import mla_workloads as mw  # noqa: E402
 # dram__bytes_read.sum + dram__bytes_write.sum of one mla_decode_kernel launch,
 # from the ncu capture summarised in profiles/mla_decode_kernel_v3.md. Drop an
 # entry whenever the kernel changes after its capture.
-MEASURED_TRAFFIC = {"v3": 366.5e6}
+MEASURED_TRAFFIC = {"v3": 365.8e6}
 METRIC = "paged MLA decode µs/step, KV GB/s & TFLOP/s as % of GB300 roofline"
 UNIT = "us/step"
 L2_FLUSH_BYTES = 512 << 20
@@ -225,29 +225,41 @@ def bench_ours(args, wl, ws, rank, local):
             m.uv_project(out, w_uv, y)
 
     parts = [prep, attend, project]
-    for _ in range(2):                      # eager warm-up (loads, first-call set-up)
+
+    def whole():
         for f in parts:
             f()
+
+    for _ in range(2):                      # eager warm-up (loads, first-call set-up)
+        whole()
     torch.cuda.synchronize()
     if not args.eager:
-        # The step as a serving loop runs it: each part captured once as a
-        # CUDA graph (the library neither allocates nor synchronises, and its
-        # tensor maps hold these fixed buffers), replayed every step.
-        graphs = []
-        for f in parts:
+        # The step as a serving loop runs it: captured once as a CUDA graph
+        # (the library neither allocates nor synchronises, and its tensor
+        # maps hold these fixed buffers) and replayed every step. Each part
+        # is also captured alone, for the breakdown.
+        def capture(f):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 f()
-            graphs.append(g)
-        parts = [g.replay for g in graphs]
+            return g.replay
+        whole_fn = capture(whole)
+        parts = [capture(f) for f in parts]
+    else:
+        whole_fn = whole
 
     def step(marks=None):
-        for k, f in enumerate(parts):
-            if marks:
-                marks[k].record(stream)
-            f()
         if marks:
-            marks[3].record(stream)
+            marks[0].record(stream)
+        whole_fn()
+        if marks:
+            marks[1].record(stream)
+
+    def step_parts(marks):
+        for k, f in enumerate(parts):
+            marks[k].record(stream)
+            f()
+        marks[3].record(stream)
 
     launches_per_step = 4 + (1 if w_uv is not None else 0)   # write, plan, split, merge (+uv)
     for _ in range(args.warmup):
@@ -256,7 +268,8 @@ def bench_ours(args, wl, ws, rank, local):
     torch.cuda.synchronize()
     assert m.get_error(wsb) == 0, "device status set during warm-up"
 
-    marks = [[ev() for _ in range(4)] for _ in range(args.steps)]
+    marks = [[ev() for _ in range(2)] for _ in range(args.steps)]
+    pmarks = [[ev() for _ in range(4)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     if ws > 1:
         torch.distributed.barrier()
@@ -268,10 +281,15 @@ def bench_ours(args, wl, ws, rank, local):
         step(marks[i])
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    step_ms = [mk[0].elapsed_time(mk[3]) for mk in marks]
-    prep_ms = [mk[0].elapsed_time(mk[1]) for mk in marks]
-    dec_ms = [mk[1].elapsed_time(mk[2]) for mk in marks]
-    uv_ms = [mk[2].elapsed_time(mk[3]) for mk in marks]
+    # The breakdown: the same steps run part by part (one graph each).
+    for i in range(args.steps):
+        flush.fill_(1)
+        step_parts(pmarks[i])
+    torch.cuda.synchronize()
+    step_ms = [mk[0].elapsed_time(mk[1]) for mk in marks]
+    prep_ms = [mk[0].elapsed_time(mk[1]) for mk in pmarks]
+    dec_ms = [mk[1].elapsed_time(mk[2]) for mk in pmarks]
+    uv_ms = [mk[2].elapsed_time(mk[3]) for mk in pmarks]
     t_step = float(np.mean(step_ms))
     t_dec = float(np.mean(dec_ms))
     if ws > 1:
@@ -347,7 +365,7 @@ def bench_ours(args, wl, ws, rank, local):
                      "traffic": args.traffic if args.traffic is not None else MEASURED_TRAFFIC.get(args.config),
                      "kernel": "mla_decode (split + merge kernels)",
                      "peak_source": peak_src + " (burst)"},
-        "launch": "eager ctypes calls" if args.eager else "one CUDA graph per part, replayed",
+        "launch": "eager ctypes calls" if args.eager else "the step replayed as one CUDA graph",
         "decode_us": t_dec * 1e3, "kv_gbs": kv_gbs, "tflops": tflops,
         "roofline_time_us": t_roof_ms * 1e3, "roofline_frac_of_step": t_roof_ms / t_step,
         "roofline_frac_of_decode": t_roof_ms / t_dec,
