@@ -172,15 +172,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   const int H = a.num_heads;
   const int ps = a.page_size;
 
-  const bool plan_ok = hd->planned == 1 && hd->batch == a.batch && hd->num_heads == a.num_heads &&
-                       hd->page_size == a.page_size && hd->window == a.window;
-  int it_begin = 0, it_end = 0;
-  if (plan_ok && cluster_id < hd->num_clusters) {
-    it_begin = cstart[cluster_id];
-    it_end = cstart[cluster_id + 1];
-  }
-  if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, MLA_STATUS_PLAN_MISMATCH);
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kBarKvFull + i), kFp8 ? 128 : 1);  // fp8: every converter thread arrives
@@ -223,6 +214,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   cluster_sync();  // barriers of both ranks initialised before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Set-up above overlaps the previous kernel (the plan); from here on the
+  // workspace, the pool and q are read.
+  pdl_wait();
+  const bool plan_ok = hd->planned == 1 && hd->batch == a.batch && hd->num_heads == a.num_heads &&
+                       hd->page_size == a.page_size && hd->window == a.window;
+  int it_begin = 0, it_end = 0;
+  if (plan_ok && cluster_id < hd->num_clusters) {
+    it_begin = cstart[cluster_id];
+    it_end = cstart[cluster_id + 1];
+  }
+  if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, MLA_STATUS_PLAN_MISMATCH);
   const int wide_x = 256 * static_cast<int>(rank);        // first c_kv dim of this rank
   const int narrow_x = 512 + 32 * static_cast<int>(rank);  // first rope dim of this rank
 
@@ -816,6 +818,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_launch_dependents();  // the merge may be scheduled as CTAs finish
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   cluster_sync();  // the peer may still address this CTA's shared memory
 }
@@ -861,8 +864,7 @@ cudaError_t launch_variant(const CUtensorMap* maps, const DecodeArgs& a, int clu
   p.q_wide = maps[2];
   p.q_narrow = maps[3];
   p.a = a;
-  mla_decode_kernel<kFp8><<<dim3(2 * clusters), dim3(C::kThreads), C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(mla_decode_kernel<kFp8>, dim3(2 * clusters), dim3(C::kThreads), C::kSmemBytes, stream, p);
 }
 
 }  // namespace

@@ -11,6 +11,7 @@
 
 #include "../../include/mla_decode.h"
 #include "mla_internal.h"
+#include "ptx.cuh"
 
 namespace mla {
 namespace {
@@ -23,6 +24,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     kv_write_kernel(uint8_t* __restrict__ layer_base, int64_t layer_rows,
                     const uint4* __restrict__ rows, const int64_t* __restrict__ slots, int n,
                     float kv_scale, int* __restrict__ status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int i = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (i >= n) return;
@@ -67,12 +70,10 @@ cudaError_t launch_kv_write(void* pool, int dtype, int64_t layer_rows, int layer
   const dim3 grid((n + kWarpsPerBlock - 1) / kWarpsPerBlock);
   const dim3 block(32 * kWarpsPerBlock);
   if (dtype == MLA_DTYPE_BF16)
-    kv_write_kernel<MLA_DTYPE_BF16><<<grid, block, 0, stream>>>(
-        base, layer_rows, static_cast<const uint4*>(rows), slots, n, kv_scale, status);
-  else
-    kv_write_kernel<MLA_DTYPE_FP8_E4M3><<<grid, block, 0, stream>>>(
-        base, layer_rows, static_cast<const uint4*>(rows), slots, n, kv_scale, status);
-  return cudaGetLastError();
+    return launch_pdl(kv_write_kernel<MLA_DTYPE_BF16>, grid, block, 0, stream, base, layer_rows,
+                      static_cast<const uint4*>(rows), slots, n, kv_scale, status);
+  return launch_pdl(kv_write_kernel<MLA_DTYPE_FP8_E4M3>, grid, block, 0, stream, base, layer_rows,
+                    static_cast<const uint4*>(rows), slots, n, kv_scale, status);
 }
 
 }  // namespace mla

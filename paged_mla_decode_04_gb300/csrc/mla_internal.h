@@ -101,6 +101,24 @@ struct DecodeArgs {
   float out_scale;   // 1, or kv_scale for fp8 pools (codes are dequantised by scaling O)
 };
 
+// Launch `kernel` on `stream` with programmatic stream serialization (see
+// pdl_wait in ptx.cuh): it may start while the previous kernel finishes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // kv_write.cu
 cudaError_t launch_kv_write(void* pool, int dtype, int64_t layer_rows, int layer, float kv_scale,
                             const void* rows, const int64_t* slots, int n, int* status,

@@ -15,6 +15,7 @@
 
 #include "../../include/mla_decode.h"
 #include "mla_internal.h"
+#include "ptx.cuh"
 
 namespace mla {
 namespace {
@@ -81,6 +82,8 @@ __global__ void __launch_bounds__(kPlanThreads)
   int* cstart = reinterpret_cast<int*>(ws + lay.cluster_start);
   SplitRequest* split = reinterpret_cast<SplitRequest*>(ws + lay.split);
   const int tid = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   if (tid == 0) bad_len = 0;
   __syncthreads();
 
@@ -278,6 +281,8 @@ constexpr int kMergeHeadsPerBlock = 4;
 __global__ void __launch_bounds__(32 * kMergeHeadsPerBlock)
     merge_kernel(const uint8_t* __restrict__ ws, WsLayout lay, int H,
                  __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const WsHeader* hd = reinterpret_cast<const WsHeader*>(ws);
   if (static_cast<int>(blockIdx.x) >= hd->num_split) return;
   const SplitRequest sr = reinterpret_cast<const SplitRequest*>(ws + lay.split)[blockIdx.x];
@@ -330,16 +335,15 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int heads, int p
   // registers; larger ones: 1024 threads looping over the batch.
   const int threads = batch <= kPlanThreads ? ((batch + 31) / 32 * 32 > 32 ? (batch + 31) / 32 * 32 : 32)
                                             : kPlanThreads;
-  plan_kernel<<<1, threads, 0, stream>>>(context_lens, batch, heads, page_size, window, clusters, ws, lay);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(threads), 0, stream, context_lens, batch, heads, page_size, window,
+                    clusters, ws, lay);
 }
 
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
   if (a.batch <= 0) return cudaSuccess;
   const dim3 grid(a.batch, (a.num_heads + kMergeHeadsPerBlock - 1) / kMergeHeadsPerBlock);
-  merge_kernel<<<grid, 32 * kMergeHeadsPerBlock, 0, stream>>>(
-      a.ws, a.lay, a.num_heads, static_cast<__nv_bfloat16*>(a.out), a.lse);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, grid, dim3(32 * kMergeHeadsPerBlock), 0, stream,
+                    static_cast<const uint8_t*>(a.ws), a.lay, a.num_heads, static_cast<__nv_bfloat16*>(a.out), a.lse);
 }
 
 }  // namespace mla

@@ -354,6 +354,15 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, 
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Kernels of the library are launched with programmatic stream
+// serialization: a kernel may be scheduled while the previous kernel on the
+// stream is still running, and must wait for it (griddepcontrol.wait: the
+// previous grid has completed and its writes are visible) before touching
+// global memory the previous kernels write, or the next ones read.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x;
   const int b0 = blockIdx.y * 128;
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -56,6 +57,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the attention output is complete
 
   if (warp == 0 && lane == 0) {
     for (int kc = 0; kc < kKChunks; ++kc) {
@@ -129,9 +131,8 @@ cudaError_t launch_uv_project(const CUtensorMap& a_map, const CUtensorMap& w_map
     attr_set = true;
   }
   const dim3 grid(heads, (batch + 127) / 128);
-  uv_project_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a_map, w_map, static_cast<__nv_bfloat16*>(y),
-                                                            batch, heads);
-  return cudaGetLastError();
+  return launch_pdl(uv_project_kernel, grid, dim3(kThreads), kSmemBytes, stream, a_map, w_map,
+                    static_cast<__nv_bfloat16*>(y), batch, heads);
 }
 
 }  // namespace mla
