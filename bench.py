@@ -56,6 +56,17 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, ws, device):
+    """Element-wise max of per-rank timings (each rank runs its own replica:
+    the job's step takes as long as its slowest rank)."""
+    if ws <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -292,10 +303,7 @@ def bench_ours(args, wl, ws, rank, local):
     uv_ms = [mk[2].elapsed_time(mk[3]) for mk in pmarks]
     t_step = float(np.mean(step_ms))
     t_dec = float(np.mean(dec_ms))
-    if ws > 1:
-        t = torch.tensor([t_step, t_dec], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_step, t_dec = float(t[0]), float(t[1])
+    t_step, t_dec = max_over_ranks([t_step, t_dec], ws, dev)
     assert m.get_error(wsb) == 0, "device status set during the timed steps"
 
     # End to end through the public API: pinned host inputs copied in, the
@@ -330,10 +338,7 @@ def bench_ours(args, wl, ws, rank, local):
         e_marks[i][1].record(stream)
     torch.cuda.synchronize()
     t_e2e = float(np.mean([a.elapsed_time(b) for a, b in e_marks]))
-    if ws > 1:
-        t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_e2e = float(t[0])
+    (t_e2e,) = max_over_ranks([t_e2e], ws, dev)
 
     if rank != 0:
         return
