@@ -60,7 +60,7 @@ constexpr int kQNarrowBytes = 128 * 64;             // [128 heads][32 rope dims]
 constexpr int kXBytes = 128 * kTile * 2;            // the peer's partial S of 128 rows, bf16
 constexpr int kF8WideBytes = kTile * 256;           // fp8 tile: [64 tokens][256 c_kv dims], unswizzled
 constexpr int kF8Bytes = kF8WideBytes + kTile * 32;  // + [64 tokens][32 rope dims]
-constexpr int kF8Stages = 4;
+constexpr int kF8Stages = 2;
 constexpr int kPvWarp = 10;
 constexpr int kCvtWarp0 = 11;                       // fp8 pools: warps 11-14 widen fp8 tiles to f16
 
@@ -70,7 +70,7 @@ constexpr int kCvtWarp0 = 11;                       // fp8 pools: warps 11-14 wi
 // sits beside it.
 template <bool kFp8>
 struct Cfg {
-  static constexpr int kStages = kFp8 ? 3 : 5;
+  static constexpr int kStages = kFp8 ? 4 : 5;
   static constexpr int kOffQn = 0;                            // q rope part, staged for TMEM
   static constexpr int kOffKV = kOffQn + kQNarrowBytes;
   static constexpr int kOffF8 = kOffKV + kStages * kStageBytes;
@@ -511,31 +511,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         if (!mbar_wait(bar(kBarF8Full + fs), fu & 1u, abort_flag)) { ok = false; break; }
         const uint32_t src = sbase + kOffF8 + fs * kF8Bytes;
         const uint32_t dst = sbase + kOffKV + stage * kStageBytes;
-        // 16 codes per unit: 64 rows x 16 units of c_kv, then 64 rows x 2 of rope.
-        for (int u = ct; u < kTile * 18; u += 128) {
-          uint32_t x[4], y[8];
-          if (u < kTile * 16) {
-            const int r = u >> 4, c = u & 15;
-            ld_shared_v4(src + r * 256 + c * 16, x[0], x[1], x[2], x[3]);
+        // 16 codes per unit: 64 rows x 16 units of c_kv, then 64 rows x 2 of
+        // rope; 1152 units, nine per thread (units ct + 128 k: eight of
+        // c_kv, one of rope). All nine are loaded first, the raw stage is
+        // released, then widened and stored.
+        static_assert(kTile * 18 == 9 * 128, "nine 16-code units per converter thread");
+        uint32_t x[9][4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              y[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k] & 0xffffu));
-              y[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k] >> 16));
-            }
+        for (int k = 0; k < 8; ++k) {
+          const int u = ct + 128 * k, r = u >> 4, c = u & 15;
+          ld_shared_v4(src + r * 256 + c * 16, x[k][0], x[k][1], x[k][2], x[k][3]);
+        }
+        {
+          const int r = ct >> 1, c = ct & 1;
+          ld_shared_v4(src + kF8WideBytes + r * 32 + c * 16, x[8][0], x[8][1], x[8][2], x[8][3]);
+        }
+        mbar_arrive(bar(kBarF8Empty + fs));  // release: the loads above are done
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+          uint32_t y[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            y[2 * j] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k][j] & 0xffffu));
+            y[2 * j + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k][j] >> 16));
+          }
+          if (k < 8) {
             // dims 16c .. 16c+15: 128-byte-swizzled chunk c / 4, 16-byte pieces 2(c % 4) and +1
+            const int u = ct + 128 * k, r = u >> 4, c = u & 15;
             const uint32_t row_base = dst + (c >> 2) * kWideBytes + r * 128;
             const int p0 = (c & 3) * 2;
             st_shared_v4(row_base + ((p0 ^ (r & 7)) << 4), y[0], y[1], y[2], y[3]);
             st_shared_v4(row_base + (((p0 + 1) ^ (r & 7)) << 4), y[4], y[5], y[6], y[7]);
           } else {
-            const int v = u - kTile * 16, r = v >> 1, c = v & 1;
-            ld_shared_v4(src + kF8WideBytes + r * 32 + c * 16, x[0], x[1], x[2], x[3]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              y[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k] & 0xffffu));
-              y[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k] >> 16));
-            }
             // rope dims 16c .. 16c+15: 64-byte-swizzled rows, pieces 2c and 2c+1
+            const int r = ct >> 1, c = ct & 1;
             const uint32_t row_base = dst + kWideChunks * kWideBytes + r * 64;
             const int sw = (r >> 1) & 3;
             st_shared_v4(row_base + (((2 * c) ^ sw) << 4), y[0], y[1], y[2], y[3]);
@@ -543,7 +552,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(bar(kBarF8Empty + fs));
         mbar_arrive(bar(kBarKvFull + stage));
       }
     }
