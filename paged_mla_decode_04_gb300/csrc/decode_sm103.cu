@@ -65,9 +65,9 @@ constexpr int kPvWarp = 10;
 constexpr int kCvtWarp0 = 11;                       // fp8 pools: warps 11-14 widen fp8 tiles to f16
 
 // Shared-memory plan of the two variants. bf16 pools: q rope part | 5-stage
-// ring of bf16 tiles | exchange | reductions | barriers. fp8 pools: the ring
-// holds the widened f16 tiles (3 stages) and a 4-stage ring of raw fp8 tiles
-// sits beside it.
+// ring of bf16 tiles | exchange | barriers. fp8 pools: the ring holds the
+// widened f16 tiles (4 stages) and a 2-stage ring of raw fp8 tiles sits
+// beside it.
 template <bool kFp8>
 struct Cfg {
   static constexpr int kStages = kFp8 ? 4 : 5;
@@ -526,7 +526,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           const int r = ct >> 1, c = ct & 1;
           ld_shared_v4(src + kF8WideBytes + r * 32 + c * 16, x[8][0], x[8][1], x[8][2], x[8][3]);
         }
-        mbar_arrive(bar(kBarF8Empty + fs));  // release: the loads above are done
+        // Release the raw slot. The fence orders the generic-proxy reads
+        // above before the slot's next TMA write (async proxy); without it
+        // the copy can land while a read is still in flight.
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarF8Empty + fs));
 #pragma unroll
         for (int k = 0; k < 9; ++k) {
           uint32_t y[8];
