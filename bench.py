@@ -255,7 +255,8 @@ def bench_ours(args, wl, ws, rank, local):
                 f()
             return g.replay
         whole_fn = capture(whole)
-        parts = [capture(f) for f in parts]
+        # (without W_UV the projection part is empty: nothing to capture)
+        parts = [capture(f) if (f is not project or w_uv is not None) else f for f in parts]
     else:
         whole_fn = whole
 
@@ -363,13 +364,16 @@ def bench_ours(args, wl, ws, rank, local):
     line = {
         "metric": METRIC, "value": t_step * 1e3, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step,
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        # tensor-core operand type: bf16 pools as stored, e4m3 pools widened to f16
+        "dtype": "bf16" if wl.dtype == mw.BF16 else "f16",
         "data": "synthetic", "config": config_dict(wl, args),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
                      "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak,
                      "traffic": args.traffic if args.traffic is not None else MEASURED_TRAFFIC.get(args.config),
                      "kernel": "mla_decode (split + merge kernels)",
-                     "peak_source": peak_src + " (burst)"},
+                     "peak_source": peak_src + " (burst)" + (
+                         "" if wl.dtype == mw.BF16 or bound == "hbm" else "; dense f16 rate = bf16 rate")},
         "launch": "eager ctypes calls" if args.eager else "the step replayed as one CUDA graph",
         "decode_us": t_dec * 1e3, "kv_gbs": kv_gbs, "tflops": tflops,
         "roofline_time_us": t_roof_ms * 1e3, "roofline_frac_of_step": t_roof_ms / t_step,
