@@ -540,12 +540,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
             y[2 * j + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(x[k][j] >> 16));
           }
           if (k < 8) {
-            // dims 16c .. 16c+15: 128-byte-swizzled chunk c / 4, 16-byte pieces 2(c % 4) and +1
+            // dims 16c .. 16c+15: 128-byte-swizzled chunk c / 4, 16-byte
+            // pieces 2(c % 4) and +1. A warp's 16-byte stores are served
+            // eight lanes at a time; lanes of odd chunks store their two
+            // pieces in the other order, so that the eight lanes of a phase
+            // (two chunks of one row) fill all eight bank groups.
             const int u = ct + 128 * k, r = u >> 4, c = u & 15;
             const uint32_t row_base = dst + (c >> 2) * kWideBytes + r * 128;
-            const int p0 = (c & 3) * 2;
-            st_shared_v4(row_base + ((p0 ^ (r & 7)) << 4), y[0], y[1], y[2], y[3]);
-            st_shared_v4(row_base + (((p0 + 1) ^ (r & 7)) << 4), y[4], y[5], y[6], y[7]);
+            const int odd = (c >> 2) & 1;
+            const int pa = (c & 3) * 2 + odd, pb = pa ^ 1;
+            st_shared_v4(row_base + ((pa ^ (r & 7)) << 4), odd ? y[4] : y[0], odd ? y[5] : y[1], odd ? y[6] : y[2],
+                         odd ? y[7] : y[3]);
+            st_shared_v4(row_base + ((pb ^ (r & 7)) << 4), odd ? y[0] : y[4], odd ? y[1] : y[5], odd ? y[2] : y[6],
+                         odd ? y[3] : y[7]);
           } else {
             // rope dims 16c .. 16c+15: 64-byte-swizzled rows, pieces 2c and 2c+1
             const int r = ct >> 1, c = ct & 1;
