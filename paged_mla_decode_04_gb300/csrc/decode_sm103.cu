@@ -34,11 +34,14 @@
 // TMEM columns: O [0, 256) fp32, q [256, 400), S [400, 464) fp32, P [464,
 // 496) bf16 pairs; S and P are single-buffered (the next QK waits for S to be
 // read, the next P for the previous PV).
-// Warp roles per CTA (352 threads; 480 for fp8 pools): warp 0 TMA producer,
-// warp 1 TMEM owner and QK issuer, warps 2-9 exchange / softmax / correction
-// / epilogue (warp w works on 16 lanes of TMEM lane quarter w & 3; a head's
-// row belongs to two threads, tokens [0, 32) and [32, 64) of each tile),
-// warp 10 PV issuer, warps 11-14 (fp8 pools) widen fp8 tiles to f16.
+// Warp roles per CTA. bf16 pools (352 threads): warp 0 TMA producer, warp 1
+// TMEM owner and QK issuer, warps 2-9 exchange / softmax / correction /
+// epilogue, warp 10 PV issuer. fp8 pools (512 threads, one role group per
+// warpgroup so that setmaxnreg can move registers to the softmax warps):
+// warps 0, 1, 2 producer, QK issuer, PV issuer (warp 3 idle), warps 4-11
+// softmax, warps 12-15 widen fp8 tiles to f16. A softmax warp w works on 16
+// lanes of TMEM lane quarter w & 3; a head's row belongs to two threads,
+// tokens [0, 32) and [32, 64) of each tile.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -61,8 +64,6 @@ constexpr int kXBytes = 128 * kTile * 2;            // the peer's partial S of 1
 constexpr int kF8WideBytes = kTile * 256;           // fp8 tile: [64 tokens][256 c_kv dims], unswizzled
 constexpr int kF8Bytes = kF8WideBytes + kTile * 32;  // + [64 tokens][32 rope dims]
 constexpr int kF8Stages = 2;
-constexpr int kPvWarp = 10;
-constexpr int kCvtWarp0 = 11;                       // fp8 pools: warps 11-14 widen fp8 tiles to f16
 
 // Shared-memory plan of the two variants. bf16 pools: q rope part | 5-stage
 // ring of bf16 tiles | exchange | barriers. fp8 pools: the ring holds the
@@ -77,7 +78,15 @@ struct Cfg {
   static constexpr int kOffX = kOffF8 + (kFp8 ? kF8Stages * kF8Bytes : 0);  // [2 buffers]
   static constexpr int kOffBar = kOffX + 2 * kXBytes;
   static constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // barriers + alignment slack
-  static constexpr int kThreads = kFp8 ? 480 : 352;
+  static constexpr int kThreads = kFp8 ? 512 : 352;
+  static constexpr int kSmWarp0 = kFp8 ? 4 : 2;    // first of the 8 softmax warps
+  static constexpr int kPvWarp = kFp8 ? 2 : 10;
+  static constexpr int kCvtWarp0 = 12;             // fp8 pools: warps 12-15 widen fp8 tiles to f16
+  // fp8 pools: registers per thread by warpgroup after setmaxnreg (producer
+  // and issuers, softmax, softmax, converters); they add up to the launch's
+  // 512 threads x 128.
+  static constexpr int kRegsIssue = 64, kRegsSoftmax = 176, kRegsCvt = 96;
+  static_assert(!kFp8 || kRegsIssue + 2 * kRegsSoftmax + kRegsCvt == 4 * 128, "register split");
   static_assert(kOffKV % 1024 == 0 && kOffF8 % 1024 == 0 && kOffX % 1024 == 0, "alignment");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kStages <= kMaxStages, "barrier arrays");
@@ -232,6 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   // 2-3, 16 KB each, on their way to TMEM), then one slot per 64-token tile.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    if constexpr (kFp8) setmaxnreg_dec<C::kRegsIssue>();
     // The whole warp walks the tiles; lane 0 issues the copies. Page ids are
     // fetched 32 at a time by the warp (one coalesced load) and handed out
     // by shuffle, so a tile waits on no global load. bf16 pools: tiles go
@@ -376,6 +386,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
+    if constexpr (kFp8) setmaxnreg_dec<C::kRegsIssue>();
     // Per item: once the previous item's QK is complete, copy q into TMEM
     // (tcgen05.cp, wide part 128 columns + rope part 16 columns); per tile:
     // S = q K^T with A read from TMEM (TS form), so shared memory streams
@@ -440,8 +451,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       mma_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, nullptr);
     }
-  } else if (warp == kPvWarp) {
+  } else if (warp == C::kPvWarp) {
     // ------------------------------------------------------------ PV issuer
+    if constexpr (kFp8) setmaxnreg_dec<C::kRegsIssue>();
     if (lane == 0) {
       const uint32_t idesc_pv = kIdescPv;
       const uint32_t tO = tmem + kColO;
@@ -471,13 +483,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       mma_commit(bar(kBarDrainPv));
       mbar_wait(bar(kBarDrainPv), 0, nullptr);
     }
-  } else if (kFp8 && warp >= kCvtWarp0) {
+  } else if (kFp8 && warp >= C::kCvtWarp0) {
     // ------------------------------------------------------------ converters (fp8 pools)
+    if constexpr (kFp8) setmaxnreg_dec<C::kRegsCvt>();
     // Per item: q's bf16 chunks and rope part become f16 in place. Per tile:
     // the raw e4m3 codes become f16 (exact: every e4m3 value is an f16) in
     // the swizzled layout the tensor core reads, the one TMA writes for bf16
     // pools. kv_scale is applied to the scores and the output instead.
-    const int ct = threadIdx.x - 32 * kCvtWarp0;  // 0..127
+    const int ct = threadIdx.x - 32 * C::kCvtWarp0;  // 0..127
     auto q_to_f16 = [&](uint32_t base, int units) {
       for (int u = ct; u < units; u += 128) {
         uint32_t x[4];
@@ -570,10 +583,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       *abort_flag = 1;
       flag_status(status, MLA_STATUS_TIMEOUT);
     }
-  } else if (warp < 2 + 8 && warp >= 2) {
+  } else if (warp >= C::kSmWarp0 && warp < C::kSmWarp0 + 8) {
     // ------------------------------------------------------------ exchange, softmax, correction, epilogue
-    // Warp w works on 16 rows (heads) of TMEM lane quarter q4 = w & 3: warps
-    // 2-5 on its lanes 0-15, warps 6-9 on lanes 16-31. A row belongs to two
+    if constexpr (kFp8) setmaxnreg_inc<C::kRegsSoftmax>();
+    // Warp w works on 16 rows (heads) of TMEM lane quarter q4 = w & 3: the
+    // first four softmax warps on its lanes 0-15, the next four on 16-31. A row belongs to two
     // threads: t and t + 16 hold its tokens [0, 32) and [32, 64) of every
     // tile (and value dims [0, 128) and [128, 256) of this rank's O), so the
     // row max and sum need one shuffle and no other warp. Per tile g: this
@@ -582,7 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     // bf16(S_0) + bf16(S_1) (fp32 addition commutes), run the same online
     // softmax and keep the same P in their own TMEM.
     const int q4 = warp & 3;
-    const int half = (warp - 2) >> 2;               // lane half of the quarter
+    const int half = (warp - C::kSmWarp0) >> 2;     // lane half of the quarter
     const int th = lane >> 4;                       // token half of a tile / value-dim half
     const int row = 32 * q4 + 16 * half + (lane & 15);
     const int nrow = min(max(H - 32 * q4 - 16 * half, 0), 16);  // valid heads of this warp
@@ -792,7 +806,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         const int tbase = blk * kTile;
         if (lo > tbase || hi < tbase + kTile) {
           const uint32_t v0 = sbase + kOffKV + (sl % kStages) * kStageBytes;
-          for (int e = threadIdx.x - 64; e < kTile * kWideChunks * 8; e += 256) {
+          for (int e = threadIdx.x - 32 * C::kSmWarp0; e < kTile * kWideChunks * 8; e += 256) {
             const int rr = e >> 5, c = (e >> 3) & 3, piece = e & 7;
             const int pos = tbase + rr;
             if (pos < lo || pos >= hi) st_shared_v4(v0 + c * kWideBytes + rr * 128 + piece * 16, 0, 0, 0, 0);
@@ -832,6 +846,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       *abort_flag = 1;
       flag_status(status, MLA_STATUS_TIMEOUT);
     }
+  } else if (kFp8) {
+    // fp8 pools: warp 3 has no role; it releases its registers with the rest
+    // of its warpgroup.
+    setmaxnreg_dec<C::kRegsIssue>();
   }
 
   tc_fence_before();
