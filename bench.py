@@ -31,9 +31,10 @@ sys.path.insert(0, ROOT)
 import mla_workloads as mw  # noqa: E402
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one mla_decode_kernel launch,
-# from the ncu capture summarised in profiles/mla_decode_kernel_v3.md. Drop an
-# entry whenever the kernel changes after its capture.
-MEASURED_TRAFFIC = {"v3": 365.8e6}
+# from the ncu captures summarised in profiles/mla_decode_kernel_v3.md and
+# profiles/mla_decode_kernel_fp8.md. Drop an entry whenever the kernel changes
+# after its capture.
+MEASURED_TRAFFIC = {"v3": 365.8e6, "fp8": 669.3e6}
 METRIC = "paged MLA decode µs/step, KV GB/s & TFLOP/s as % of GB300 roofline"
 UNIT = "us/step"
 L2_FLUSH_BYTES = 512 << 20
