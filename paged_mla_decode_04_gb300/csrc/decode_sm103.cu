@@ -140,11 +140,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
-  tmem_st16(taddr, r);
-  tmem_st16(taddr + 16, r + 16);
-}
-
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ Params p) {
