@@ -331,3 +331,28 @@ def test_full_size_repeated_runs_are_bit_identical(lib, name):
         out, lse = dw.step(write=False)
         assert np.array_equal(out, out0) and np.array_equal(lse, lse0)
     assert lib.get_error(dw.ws) == 0
+
+
+@pytest.mark.parametrize("batch", [1024, 1100, 2100])
+def test_large_batches_take_both_plan_paths(lib, batch):
+    """Up to 1024 requests the plan keeps one request per thread in registers;
+    beyond it loops over the batch in chunks of 1024 through the workspace.
+    Short ragged lengths (tile edges included) over every cluster; every
+    request checked against the oracle."""
+    rng = np.random.default_rng(batch)
+    lens = rng.integers(0, 200, size=batch).astype(np.int32)
+    lens[:5] = [0, 1, 63, 64, 65]
+    wl = mw.make("v2lite", num_heads=16, context_lens=lens)
+    dw = DeviceWorkload(wl, lib)
+    out, lse = dw.step()
+    ref_out, ref_lse = oracle_step(wl)
+    _check(out, lse, ref_out, ref_lse)
+    assert lib.get_error(dw.ws) == 0
+
+
+def test_empty_batch_is_a_no_op(lib):
+    wl = mw.make("v2lite", context_lens=np.zeros(0, np.int32))
+    dw = DeviceWorkload(wl, lib)
+    out, lse = dw.step()
+    assert out.shape == (0, wl.num_heads, mw.D_CKV) and lse.shape == (0, wl.num_heads)
+    assert lib.get_error(dw.ws) == 0
