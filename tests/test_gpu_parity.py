@@ -260,8 +260,8 @@ def test_uv_project(lib, batch, heads):
 
 # ----------------------------------------------------------------- fp8 e4m3 cache
 
-@pytest.mark.parametrize("heads", [16, 64, 128])
-@pytest.mark.parametrize("ps", [16, 64, 128])
+@pytest.mark.parametrize("heads", [16, 32, 64, 128])
+@pytest.mark.parametrize("ps", [16, 32, 64, 128])
 def test_fp8_cache_ragged_lengths(lib, heads, ps):
     lens = [0, 1, 63, 64, 65, 200, 777]
     wl = mw.make("fp8", num_heads=heads, context_lens=lens, page_size=ps)
@@ -270,6 +270,17 @@ def test_fp8_cache_ragged_lengths(lib, heads, ps):
     ref_out, ref_lse = oracle_step(wl)
     _check(out, lse, ref_out, ref_lse, tol=TOL_FP8)
     assert lib.get_error(dw.ws) == 0
+
+
+def test_fp8_cache_csr_equals_block_table(lib):
+    lens = [17, 640, 1999, 0, 65]
+    wl = mw.make("fp8", num_heads=64, context_lens=lens, page_size=16)
+    dw = DeviceWorkload(wl, lib)
+    out_t, lse_t = dw.step()
+    out_c, lse_c = dw.step(csr=True, write=False)
+    assert np.array_equal(out_t, out_c) and np.array_equal(lse_t, lse_c)
+    ref_out, ref_lse = oracle_step(wl)
+    _check(out_c, lse_c, ref_out, ref_lse, tol=TOL_FP8)
 
 
 @pytest.mark.parametrize("window,clusters", [(0, 7), (100, 0), (1, 2)])
