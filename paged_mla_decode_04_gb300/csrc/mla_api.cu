@@ -187,7 +187,7 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = mla::launch_decode(maps, a, cmax, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  e = mla::launch_merge(a, st);
+  e = mla::launch_merge(a, cmax, st);
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -127,7 +127,7 @@ cudaError_t launch_kv_write(void* pool, int dtype, int64_t layer_rows, int layer
 cudaError_t launch_plan(const int32_t* context_lens, int batch, int heads, int page_size,
                         int window, int clusters, uint8_t* ws, const WsLayout& lay,
                         cudaStream_t stream);
-cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeArgs& a, int clusters, cudaStream_t stream);
 // decode_sm103.cu
 // maps: {kv 64-dim boxes (128B swizzle), kv 32-dim boxes (64B swizzle),
 //        q 64-dim boxes, q 32-dim boxes}

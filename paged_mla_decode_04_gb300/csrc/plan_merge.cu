@@ -279,11 +279,15 @@ constexpr int kMergeHeadsPerBlock = 4;
 // out[b,h] = sum_s 2^(lse_s - m) O_s / sum_s 2^(lse_s - m), O_s normalised
 // per split, lse in log2 units; the natural-log lse is reported.
 __global__ void __launch_bounds__(32 * kMergeHeadsPerBlock)
-    merge_kernel(const uint8_t* __restrict__ ws, WsLayout lay, int H,
+    merge_kernel(uint8_t* __restrict__ ws, WsLayout lay, int H,
                  __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
   pdl_launch_dependents();
   pdl_wait();
-  const WsHeader* hd = reinterpret_cast<const WsHeader*>(ws);
+  WsHeader* hd = reinterpret_cast<WsHeader*>(ws);
+  // The grid covers at most min(batch, clusters) split requests; a schedule
+  // with more would leave some unmerged, so it is reported.
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && hd->num_split > static_cast<int>(gridDim.x))
+    atomicOr(&hd->status, MLA_STATUS_PLAN_MISMATCH);
   if (static_cast<int>(blockIdx.x) >= hd->num_split) return;
   const SplitRequest sr = reinterpret_cast<const SplitRequest*>(ws + lay.split)[blockIdx.x];
   const int lane = threadIdx.x & 31;
@@ -339,11 +343,14 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int heads, int p
                     clusters, ws, lay);
 }
 
-cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_merge(const DecodeArgs& a, int clusters, cudaStream_t stream) {
   if (a.batch <= 0) return cudaSuccess;
-  const dim3 grid(a.batch, (a.num_heads + kMergeHeadsPerBlock - 1) / kMergeHeadsPerBlock);
+  // A split request holds one of the schedule's cluster boundaries (fewer
+  // than `clusters`), so at most min(batch, clusters) requests are split.
+  const int rows = a.batch < clusters ? a.batch : clusters;
+  const dim3 grid(rows, (a.num_heads + kMergeHeadsPerBlock - 1) / kMergeHeadsPerBlock);
   return launch_pdl(merge_kernel, grid, dim3(32 * kMergeHeadsPerBlock), 0, stream,
-                    static_cast<const uint8_t*>(a.ws), a.lay, a.num_heads, static_cast<__nv_bfloat16*>(a.out), a.lse);
+                    a.ws, a.lay, a.num_heads, static_cast<__nv_bfloat16*>(a.out), a.lse);
 }
 
 }  // namespace mla
