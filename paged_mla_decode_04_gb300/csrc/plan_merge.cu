@@ -275,9 +275,12 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 constexpr int kMergeHeadsPerBlock = 4;
+constexpr int kMergeBatch = 4;  // partials whose loads are issued together
 
 // out[b,h] = sum_s 2^(lse_s - m) O_s / sum_s 2^(lse_s - m), O_s normalised
-// per split, lse in log2 units; the natural-log lse is reported.
+// per split, lse in log2 units; the natural-log lse is reported. The loads
+// of the first kMergeBatch partials (lse and O) are issued together, so the
+// chain of dependent global loads is short; the sums run in split order.
 __global__ void __launch_bounds__(32 * kMergeHeadsPerBlock)
     merge_kernel(uint8_t* __restrict__ ws, WsLayout lay, int H,
                  __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
@@ -285,35 +288,60 @@ __global__ void __launch_bounds__(32 * kMergeHeadsPerBlock)
   pdl_wait();
   WsHeader* hd = reinterpret_cast<WsHeader*>(ws);
   // The grid covers at most min(batch, clusters) split requests; a schedule
-  // with more would leave some unmerged, so it is reported.
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && hd->num_split > static_cast<int>(gridDim.x))
-    atomicOr(&hd->status, MLA_STATUS_PLAN_MISMATCH);
-  if (static_cast<int>(blockIdx.x) >= hd->num_split) return;
+  // with more would leave some unmerged, so it is reported. The split table
+  // holds `batch` records, so the record of this row is read in the same
+  // step as the count and used only when the row is in range.
+  const int num_split = hd->num_split;
   const SplitRequest sr = reinterpret_cast<const SplitRequest*>(ws + lay.split)[blockIdx.x];
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && num_split > static_cast<int>(gridDim.x))
+    atomicOr(&hd->status, MLA_STATUS_PLAN_MISMATCH);
+  if (static_cast<int>(blockIdx.x) >= num_split) return;
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y * kMergeHeadsPerBlock + (threadIdx.x >> 5);
   if (h >= H) return;
   const float* plse = reinterpret_cast<const float*>(ws + lay.partial_lse);
   const float* po = reinterpret_cast<const float*>(ws + lay.partial_o);
+  const int ns = sr.num_splits;
+  auto src = [&](int s) {
+    return reinterpret_cast<const float4*>(po + (static_cast<size_t>(sr.first_partial + s) * H + h) * kDimCkv);
+  };
+  float lv[kMergeBatch];
+  float4 v[kMergeBatch][4];
+#pragma unroll
+  for (int k = 0; k < kMergeBatch; ++k) {
+    if (k < ns) {
+      lv[k] = plse[(sr.first_partial + k) * H + h];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[k][j] = src(k)[lane + 32 * j];
+    }
+  }
   float m = -CUDART_INF_F;
-  for (int s = 0; s < sr.num_splits; ++s) m = fmaxf(m, plse[(sr.first_partial + s) * H + h]);
+#pragma unroll
+  for (int k = 0; k < kMergeBatch; ++k)
+    if (k < ns) m = fmaxf(m, lv[k]);
+  for (int s = kMergeBatch; s < ns; ++s) m = fmaxf(m, plse[(sr.first_partial + s) * H + h]);
   float4 acc[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  for (int s = 0; s < sr.num_splits; ++s) {
-    const int p = sr.first_partial + s;
-    const float w = exp2f(plse[p * H + h] - m);
+  auto add = [&](float w, const float4* x) {
     wsum += w;
-    const float4* src = reinterpret_cast<const float4*>(po + (static_cast<size_t>(p) * H + h) * kDimCkv);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float4 v = src[lane + 32 * j];
-      acc[j].x += w * v.x;
-      acc[j].y += w * v.y;
-      acc[j].z += w * v.z;
-      acc[j].w += w * v.w;
+      acc[j].x += w * x[j].x;
+      acc[j].y += w * x[j].y;
+      acc[j].z += w * x[j].z;
+      acc[j].w += w * x[j].w;
     }
+  };
+#pragma unroll
+  for (int k = 0; k < kMergeBatch; ++k)
+    if (k < ns) add(exp2f(lv[k] - m), v[k]);
+  for (int s = kMergeBatch; s < ns; ++s) {
+    float4 x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = src(s)[lane + 32 * j];
+    add(exp2f(plse[(sr.first_partial + s) * H + h] - m), x);
   }
   const float inv = 1.f / wsum;
   __nv_bfloat16* dst = out + (static_cast<size_t>(sr.b) * H + h) * kDimCkv;
