@@ -30,14 +30,25 @@ sys.path.insert(0, ROOT)
 
 import mla_workloads as mw  # noqa: E402
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one mla_decode_kernel launch,
-# from the ncu captures summarised in profiles/mla_decode_kernel_v3.md and
-# profiles/mla_decode_kernel_fp8.md. Drop an entry whenever the kernel changes
-# after its capture.
-MEASURED_TRAFFIC = {"v3": 365.8e6, "fp8": 669.3e6}
+# dram__bytes_read.sum + dram__bytes_write.sum of one mla_decode_kernel launch
+# from an ncu capture, keyed by workload and by the digest of the decode
+# kernel's sources at capture time (decode_source_digest): the figure is
+# printed only for the kernel it was measured on, null for any other.
+MEASURED_TRAFFIC = {}
+DECODE_SOURCES = ["decode_sm103.cu", "ptx.cuh", "mla_internal.h", "trace.cuh"]
 METRIC = "paged MLA decode µs/step, KV GB/s & TFLOP/s as % of GB300 roofline"
 UNIT = "us/step"
 L2_FLUSH_BYTES = 512 << 20
+
+
+def decode_source_digest() -> str:
+    """Short digest of the decode kernel's source files."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_mla_decode_04_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def load_peaks():
@@ -234,7 +245,7 @@ def bench_ours(args, wl, ws, rank, local):
 
     def project():
         if w_uv is not None:
-            m.uv_project(out, w_uv, y)
+            m.uv_project(out, w_uv, y, wsb)
 
     parts = [prep, attend, project]
 
@@ -371,7 +382,9 @@ def bench_ours(args, wl, ws, rank, local):
         "data": "synthetic", "config": config_dict(wl, args),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
                      "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak,
-                     "traffic": args.traffic if args.traffic is not None else MEASURED_TRAFFIC.get(args.config),
+                     "traffic": args.traffic if args.traffic is not None else MEASURED_TRAFFIC.get(
+                         (args.config, decode_source_digest())),
+                     "kernel_digest": decode_source_digest(),
                      "kernel": "mla_decode (split + merge kernels)",
                      "peak_source": peak_src + " (burst)" + (
                          "" if wl.dtype == mw.BF16 or bound == "hbm" else "; dense f16 rate = bf16 rate")},

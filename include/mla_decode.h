@@ -162,10 +162,15 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q,
 /* W_UV projection after attention: y[b,h,:] = attn_out[b,h,:] @ w_uv[h],
  * v_head_dim 128 (MoE-Infinity PR #195, Root causes 3).
  *   attn_out: device [batch][num_heads][512] bf16; w_uv: device
- *   [num_heads][512][128] bf16; y: device [batch][num_heads][128] bf16.
+ *   [num_heads][512][128] bf16; y: device [batch][num_heads][128] bf16; all
+ *   16-byte aligned (MLA_ERR_ARG otherwise).
+ *   workspace: a decode workspace (256-byte aligned) whose status word
+ *   records MLA_STATUS_TIMEOUT if a bounded wait inside the kernel runs out,
+ *   or NULL. Either way the rows such a wait leaves unfinished are written
+ *   as NaN, never left stale.
  * fp32 accumulation. */
 int mla_uv_project(const void* attn_out, const void* w_uv, void* y, int batch,
-                   int num_heads, void* stream);
+                   int num_heads, void* workspace, void* stream);
 
 /* Reads the status word of `workspace` into *code (MLA_STATUS_* bits) and, if
  * `clear` is nonzero, resets it. Synchronises `stream`: diagnostics only. */
@@ -175,7 +180,7 @@ int mla_get_error(void* workspace, int* code, int clear, void* stream);
  * all: code running inside a memory pool or arena that it does not own,
  * plugins whose host forbids cudaMalloc while a graph or a tight memory
  * budget is active, or embedded runtimes that only hand out fixed buffers.
- * The paper has no counterpart of this call; it is the same operation as
+ * The published method has no counterpart of this call; it is the same operation as
  * mla_decode_plan followed by mla_decode (same arguments, same results),
  * with the schedule and the split partials kept in a scratch array that the
  * library declares at file scope (MLA_NOALLOC_SCRATCH_BYTES of device

@@ -135,9 +135,13 @@ SEEDS = {"tiny": 1235, "v2lite": 1236, "v3": 1237, "fp8": 1238, "long": 1239,
 def make(name: str, seed: Optional[int] = None, batch: Optional[int] = None,
          num_heads: Optional[int] = None, context_lens=None, page_size: Optional[int] = None,
          window: Optional[int] = None, num_layers: int = 2, layer: int = 1,
-         spare_pages: int = SPARE_PAGES) -> Workload:
-    """Build one seeded workload. Overrides shrink a configuration for tests."""
+         spare_pages: int = SPARE_PAGES, value_std: Optional[float] = None,
+         q_std: float = 1.0) -> Workload:
+    """Build one seeded workload. Overrides shrink a configuration for tests;
+    value_std and q_std change the spread of the cache values and of q (for
+    score scales like a trained model's, where the softmax is peaked)."""
     B0, H0, ps0, dtype, W0, std, has_uv = CONFIGS[name]
+    std = std if value_std is None else value_std
     seed = SEEDS[name] if seed is None else seed
     rng = np.random.default_rng(seed)
     H = H0 if num_heads is None else num_heads
@@ -160,7 +164,7 @@ def make(name: str, seed: Optional[int] = None, batch: Optional[int] = None,
     for b in range(B):
         block_table[b, : n_blocks[b]] = ids[indptr[b]: indptr[b + 1]]
     pool = _normal_bf16(rng, (num_layers, P, ps, D_ROW), std)
-    q = _normal_bf16(rng, (B, H, D_ROW), 1.0)
+    q = _normal_bf16(rng, (B, H, D_ROW), q_std)
     new_rows = _normal_bf16(rng, (B, D_ROW), std)
     slots = np.array([int(block_table[b, L[b] // ps]) * ps + int(L[b]) % ps for b in range(B)],
                      np.int64)

@@ -10,7 +10,7 @@ Calls (same names as the C ABI in include/mla_decode.h):
   plan(context_lens, num_heads, page_size, window, workspace, num_clusters=0)
   decode(pool, layer, q, context_lens, softmax_scale, workspace, out,
          block_table=None | page_indptr + page_ids, window=0, lse=None)
-  uv_project(attn_out, w_uv, y)
+  uv_project(attn_out, w_uv, y, workspace=None)
   get_error(workspace, clear=False)
 """
 from __future__ import annotations
@@ -77,7 +77,7 @@ def load_library(path: str = LIB_PATH):
     lib.mla_decode.argtypes = [ctypes.POINTER(_Pool), I, P, P, P, I, P, I, I, ctypes.c_float, I,
                                P, P, P, P]
     lib.mla_decode.restype = I
-    lib.mla_uv_project.argtypes = [P, P, P, I, I, P]
+    lib.mla_uv_project.argtypes = [P, P, P, I, I, P, P]
     lib.mla_uv_project.restype = I
     lib.mla_get_error.argtypes = [P, ctypes.POINTER(I), I, P]
     lib.mla_get_error.restype = I
@@ -207,7 +207,8 @@ def decode(pool: KVPool, layer: int, q: torch.Tensor, context_lens: torch.Tensor
     return out
 
 
-def uv_project(attn_out: torch.Tensor, w_uv: torch.Tensor, y: torch.Tensor, stream=None):
+def uv_project(attn_out: torch.Tensor, w_uv: torch.Tensor, y: torch.Tensor,
+               workspace: Optional[torch.Tensor] = None, stream=None):
     lib = load_library()
     B, H, D = attn_out.shape
     if D != KV_LORA_RANK or w_uv.shape != (H, KV_LORA_RANK, V_HEAD_DIM) or \
@@ -215,6 +216,7 @@ def uv_project(attn_out: torch.Tensor, w_uv: torch.Tensor, y: torch.Tensor, stre
         raise ValueError("attn_out [B,H,512], w_uv [H,512,128], y [B,H,128] expected")
     rc = lib.mla_uv_project(_dev(attn_out, "attn_out", torch.bfloat16),
                             _dev(w_uv, "w_uv", torch.bfloat16), _dev(y, "y", torch.bfloat16), B, H,
+                            None if workspace is None else _dev(workspace, "workspace"),
                             _stream(stream))
     _check(rc, "mla_uv_project")
     return y

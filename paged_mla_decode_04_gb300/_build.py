@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmla_decode.so")
 SOURCES = ["mla_api.cu", "kv_write.cu", "plan_merge.cu", "decode_sm103.cu", "uv_project.cu"]
-HEADERS = ["ptx.cuh", "mla_internal.h"]
+HEADERS = ["ptx.cuh", "mla_internal.h", "trace.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -40,17 +40,21 @@ def _stale(target, inputs):
     return any(os.path.getmtime(i) > t for i in inputs)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, defines=(),
+          lib_path: str = LIB, build_dir: str = BUILD) -> str:
+    """Compile every kernel file and link libmla_decode.so (only what is stale).
+    `defines` (e.g. ["-DMLA_TRACE"] for the event-traced build) go with
+    their own lib_path and build_dir."""
+    os.makedirs(build_dir, exist_ok=True)
     deps = _deps()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-                    "--expt-relaxed-constexpr"]
+                    "--expt-relaxed-constexpr", *defines]
     if ptxas_info:
         flags += ["-Xptxas", "-v"]
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or ptxas_info or _stale(o, [s] + deps):
             jobs.append([nvcc(), *flags, "-c", s, "-o", o])
@@ -65,11 +69,11 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for log in ex.map(run, jobs):
             if verbose and log:
                 print(log)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp.%d" % os.getpid()
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + ".tmp.%d" % os.getpid()
         run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

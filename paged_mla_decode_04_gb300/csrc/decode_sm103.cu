@@ -48,6 +48,7 @@
 #include "../../include/mla_decode.h"
 #include "mla_internal.h"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace mla {
 namespace {
@@ -175,6 +176,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   const int cluster_id = blockIdx.x >> 1;
   const int H = a.num_heads;
   const int ps = a.page_size;
+  if (threadIdx.x == 0) MLA_TRACE_EVENT(5, kEvKernelStart, 0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -229,6 +231,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     it_end = cstart[cluster_id + 1];
   }
   if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, MLA_STATUS_PLAN_MISMATCH);
+  if (threadIdx.x == 0) MLA_TRACE_EVENT(5, kEvSetupDone, it_end - it_begin);
   const int wide_x = 256 * static_cast<int>(rank);        // first c_kv dim of this rank
   const int narrow_x = 512 + 32 * static_cast<int>(rank);  // first rope dim of this rank
 
@@ -251,7 +254,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     uint32_t sl = 0;     // ring slot
     uint32_t ft = 0;     // fp8 ring slot
     int last_qn_item = -1, last_q_item = -1, last_q_chunks = 0;
-    uint32_t n_items = 0;
+    uint32_t n_items = 0, gt = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
       const WorkItem w = items[it];
@@ -339,6 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         ++sl;
         if (!ok) break;
         if (lane == 0) {
+          MLA_TRACE_EVENT(0, kEvSlotAcquired, gt);
           mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(nbox * rows_per_box) * row_bytes);
 #pragma unroll
           for (int bx = 0; bx < 4; ++bx) {
@@ -355,7 +359,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
                                narrow_x, rows[bx], kv_policy);
             }
           }
+          MLA_TRACE_EVENT(0, kEvTileIssued, gt);
         }
+        ++gt;
       }
     }
     if (lane == 0) {
@@ -415,11 +421,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         mma_commit(bar(kBarKvEmpty + s0));
         mma_commit(bar(kBarKvEmpty + s1));
         mma_commit(bar(kBarQnFree));
+        MLA_TRACE_EVENT(1, kEvQLoaded, g);
         sl += 2;
         for (int t = 0; t < nt; ++t, ++g, ++sl) {
           const uint32_t stage = sl % kStages, use = sl / kStages;
           if (!mbar_wait(bar(kBarKvFull + stage), use & 1u, abort_flag)) { ok = false; break; }
+          MLA_TRACE_EVENT(1, kEvQkTileReady, g);
           if (!mbar_wait(bar(kBarSFree), (g & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+          MLA_TRACE_EVENT(1, kEvQkSFree, g);
           tc_fence_after();
           const uint32_t kv = sbase + kOffKV + stage * kStageBytes;
           // Descriptors of the tile's first chunk; the others differ only in
@@ -436,6 +445,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           for (int k = 0; k < 2; ++k)
             mma_bf16_ts(tS, tQ + 128u + 8u * k, dn + static_cast<uint64_t>((k * 32) >> 4), idesc_qk, 1u);
           mma_commit(bar(kBarSFull));
+          MLA_TRACE_EVENT(1, kEvQkIssued, g);
         }
         if (ok) mma_commit(bar(kBarQDone));  // every QK of this item complete: q may be replaced
       }
@@ -460,6 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         sl += 2;
         for (int t = 0; t < nt; ++t, ++g, ++sl) {
           if (!mbar_wait(bar(kBarOFixed), g & 1u, abort_flag)) { ok = false; break; }
+          MLA_TRACE_EVENT(2, kEvPvOFixed, g);
           tc_fence_after();
           fence_proxy_async_smem();
           const uint64_t dv = sdesc_sw128(sbase + kOffKV + (sl % kStages) * kStageBytes, kWideBytes, 1024);
@@ -469,6 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
                         (t | k) != 0);
           mma_commit(bar(kBarKvEmpty + sl % kStages));
           mma_commit(bar(kBarPvDone));
+          MLA_TRACE_EVENT(2, kEvPvIssued, g);
         }
       }
       if (!ok) {
@@ -600,6 +612,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     const uint32_t tO = tmem + lane_base + kColO;   // this warp's 16 rows of O
     const uint32_t dim0 = 256u * rank + 128u * th;  // first value dim of this thread
     constexpr int kHalf = kTile / 2;
+    const bool tracer = lane == 0 && (warp == C::kSmWarp0 || warp == C::kSmWarp0 + 7);
+    auto tr = [&](uint32_t ev, uint32_t t) {
+      if (tracer) MLA_TRACE_EVENT(warp == C::kSmWarp0 ? 3 : 4, ev, t);
+    };
     auto wwait = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(b, parity, abort_flag));
     };
@@ -619,6 +635,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     // Epilogue of an item: wait for its last PV, normalise this thread's
     // 128 value dims, store.
     auto store_item = [&](const WorkItem& w, uint32_t g_last, float m, float l) -> bool {
+      tr(kEvSmItemStore, g_last);
       if (!wwait(bar(kBarPvDone), g_last & 1u)) return false;
       tc_fence_after();
       if (rank == 0 && th == 0 && valid) {
@@ -658,6 +675,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         }
       }
       tc_fence_before();
+      tr(kEvSmItemStored, g_last);
       return true;
     };
     // Software pipeline: the partial scores of tile g+1 are fetched from TMEM
@@ -671,6 +689,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     auto fetch = [&](uint32_t gg, uint32_t* xp) -> bool {
       const uint32_t b = gg & 1u, u = gg >> 1;
       if (!wwait(bar(kBarSFull), gg & 1u)) return false;
+      tr(kEvSmSFull, gg);
       tc_fence_after();
       if (nrow > 0) {
         uint32_t r[kHalf];
@@ -678,7 +697,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         tmem_ld_h16<kHalf>(tmem + lane_base + kColS + 16, r + 16);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < kHalf / 2; ++i) xp[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        for (int i = 0; i < kHalf / 2; ++i)
+          xp[i] = pack_f16x2(__uint_as_float(r[2 * i]) * a.scale_log2, __uint_as_float(r[2 * i + 1]) * a.scale_log2);
       }
       tc_fence_before();
       mbar_arrive(bar(kBarSFree));
@@ -693,6 +713,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         }
         if (lane == 0) mbar_arrive_expect_tx(xfull(b), static_cast<uint32_t>(2 * nrow * kHalf * 2));
       }
+      tr(kEvSmSent, gg);
       return true;
     };
     // Fetching S(g+1) needs its ring slot, whose previous tile must have
@@ -727,6 +748,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         uint32_t pk[kHalf / 2];
         if (nrow > 0) {
           if (!wwait_cluster(xfull(b), u & 1u)) { ok = false; break; }
+          tr(kEvSmXFull, g);
           // Scores as packed fp32 pairs (tokens 2i, 2i+1): both ranks add the
           // same two bf16 partials.
           uint64_t s2[kHalf / 2];
@@ -737,7 +759,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
               uint32_t x[4];
               ld_shared_v4(xq(b) + (j * 32 + lane) * 16, x[0], x[1], x[2], x[3]);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) s2[4 * j + k] = f2_add(f2_from_bf16x2(xp[4 * j + k]), f2_from_bf16x2(x[k]));
+              for (int k = 0; k < 4; ++k) s2[4 * j + k] = f2_add(f2_from_f16x2(xp[4 * j + k]), f2_from_f16x2(x[k]));
             }
           }
           __syncwarp();
@@ -762,23 +784,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
               mx4[(2 * i + 1) & 3] = fmaxf(mx4[(2 * i + 1) & 3], s1);
             }
           }
-          // The row max over both token halves (scores are scaled by a
-          // positive factor, so the max of the raw sums is taken).
+          // The row max over both token halves (the partials were scaled to
+          // log2 units before the exchange).
           float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * a.scale_log2;
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           if (valid) {
             if (mx > m + kRescaleThreshold) {
               alpha = fast_exp2(m - mx);  // 0 on the first tile (m = -inf)
               l *= alpha;
               m = mx;
             }
-            const uint64_t c2 = f2_make(a.scale_log2, a.scale_log2);
             const uint64_t nm2 = f2_make(-m, -m);
             uint64_t rs2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) {
               float t0, t1;
-              f2_split(f2_fma(s2[i], c2, nm2), t0, t1);
+              f2_split(f2_add(s2[i], nm2), t0, t1);
               const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
               rs2[i & 1] = f2_add(rs2[i & 1], f2_make(p0, p1));
               pk[i] = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
@@ -787,6 +808,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
             f2_split(rs2[0], r0, r1);
             f2_split(rs2[1], r2, r3);
             l += (r0 + r1) + (r2 + r3);
+            tr(kEvSmComputed, g);
           } else {
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) pk[i] = 0;
@@ -811,6 +833,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         // TMEM P and O are free once PV(g-1) is done. Waiting here also keeps
         // a warp without heads from arriving twice in one phase of OFixed.
         if (!wwait(bar(kBarPvDone), (g & 1u) ^ 1u)) { ok = false; break; }
+        tr(kEvSmPvDone, g);
         tc_fence_after();
         if (nrow > 0) {
           tmem_st_h16<kHalf / 2>(tmem + lane_base + kColP, pk);
@@ -831,6 +854,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         }
         tc_fence_before();
         mbar_arrive(bar(kBarOFixed));
+        tr(kEvSmOFixed, g);
       }
       if (!ok) break;
       // The row sum over both token halves.
@@ -847,6 +871,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     setmaxnreg_dec<C::kRegsIssue>();
   }
 
+  if (threadIdx.x == 0) MLA_TRACE_EVENT(5, kEvKernelEnd, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -883,13 +908,9 @@ int max_active_clusters_of() {
 template <bool kFp8>
 cudaError_t launch_variant(const CUtensorMap* maps, const DecodeArgs& a, int clusters, cudaStream_t stream) {
   using C = Cfg<kFp8>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static bool attr_set[kMaxDevices] = {};
+  const cudaError_t e = set_smem_once(mla_decode_kernel<kFp8>, C::kSmemBytes, attr_set);
+  if (e != cudaSuccess) return e;
   Params p;
   p.kv_wide = maps[0];
   p.kv_narrow = maps[1];
@@ -901,15 +922,18 @@ cudaError_t launch_variant(const CUtensorMap* maps, const DecodeArgs& a, int clu
 
 }  // namespace
 
-// Co-resident clusters: the smaller of the two variants' counts, so that one
-// plan serves either pool type.
+// Co-resident clusters on the current device: the smaller of the two
+// variants' counts, so that one plan serves either pool type (cached per
+// device).
 int decode_max_active_clusters() {
-  static int cached = -1;
-  if (cached > 0) return cached;
+  static int cached[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0) return -1;
+  if (cached[dev] > 0) return cached[dev];
   const int a = max_active_clusters_of<false>(), b = max_active_clusters_of<true>();
   if (a <= 0 || b <= 0) return -1;
-  cached = a < b ? a : b;
-  return cached;
+  cached[dev] = a < b ? a : b;
+  return cached[dev];
 }
 
 cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& a, int clusters, cudaStream_t stream) {
@@ -918,3 +942,15 @@ cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& a, int clus
 }
 
 }  // namespace mla
+
+#ifdef MLA_TRACE
+// Copies the trace buffer to the host ([ctas][roles][cap] records and
+// [ctas][roles] counts) and clears the counts. Traced builds only.
+extern "C" int mla_trace_read(void* records, void* counts) {
+  if (cudaMemcpyFromSymbol(records, mla::g_trace, sizeof(mla::g_trace)) != cudaSuccess) return -4;
+  if (cudaMemcpyFromSymbol(counts, mla::g_trace_n, sizeof(mla::g_trace_n)) != cudaSuccess) return -4;
+  static uint32_t zero[mla::kTraceCtas][mla::kTraceRoles] = {};
+  if (cudaMemcpyToSymbol(mla::g_trace_n, zero, sizeof(zero)) != cudaSuccess) return -4;
+  return 0;
+}
+#endif

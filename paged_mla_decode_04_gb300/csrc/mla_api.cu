@@ -59,6 +59,22 @@ bool valid_pool(const mla_kv_pool* pool) {
 
 int max_clusters() { return mla::decode_max_active_clusters(); }
 
+// The host-visible checks of mla_decode (everything but the workspace), so
+// that mla_decode_noalloc can run them before it touches its scratch.
+int check_decode_args(const mla_kv_pool* pool, int layer, const void* q, const int32_t* page_indptr,
+                      const int32_t* page_ids, int max_blocks, const int32_t* context_lens, int batch,
+                      int num_heads, float softmax_scale, int window, const void* out) {
+  if (!valid_pool(pool) || layer < 0 || layer >= pool->num_layers || batch < 0 || window < 0) return MLA_ERR_ARG;
+  if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
+  if (batch == 0) return MLA_OK;
+  if (!q || !page_ids || !context_lens || !out || !aligned(q, 16) || !aligned(out, 32)) return MLA_ERR_ARG;
+  if (!page_indptr && max_blocks <= 0) return MLA_ERR_ARG;
+  if (!(softmax_scale > 0.f)) return MLA_ERR_ARG;
+  const uint64_t total_rows = static_cast<uint64_t>(pool->num_layers) * pool->num_pages * pool->page_size;
+  if (total_rows >= (1ull << 31)) return MLA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+  return MLA_OK;
+}
+
 // Device address of g_noalloc_scratch on the current device, looked up once
 // per device (the host-side symbol is only a stand-in for it).
 void* noalloc_scratch() {
@@ -121,20 +137,16 @@ int mla_decode_plan(const int32_t* context_lens, int batch, int num_heads, int p
 int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t* page_indptr,
                const int32_t* page_ids, int max_blocks, const int32_t* context_lens, int batch, int num_heads,
                float softmax_scale, int window, void* workspace, void* out, float* lse, void* stream) {
-  if (!valid_pool(pool) || layer < 0 || layer >= pool->num_layers || batch < 0 || window < 0 || !workspace)
-    return MLA_ERR_ARG;
-  if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
-  if (batch == 0) return MLA_OK;
-  if (!q || !page_ids || !context_lens || !out || !aligned(q, 16) || !aligned(out, 32)) return MLA_ERR_ARG;
-  if (!page_indptr && max_blocks <= 0) return MLA_ERR_ARG;
-  if (!(softmax_scale > 0.f)) return MLA_ERR_ARG;
+  if (!workspace) return MLA_ERR_ARG;
+  const int rc = check_decode_args(pool, layer, q, page_indptr, page_ids, max_blocks, context_lens, batch,
+                                   num_heads, softmax_scale, window, out);
+  if (rc != MLA_OK || batch == 0) return rc;
   const int cmax = max_clusters();
   if (cmax <= 0) return MLA_ERR_CUDA;
   if (!aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
 
   const int ps = pool->page_size;
   const uint64_t total_rows = static_cast<uint64_t>(pool->num_layers) * pool->num_pages * ps;
-  if (total_rows >= (1ull << 31)) return MLA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
   // Each rank of the decode cluster reads its 256 c_kv dims and 32 rope
   // dims of every row: bf16 pools as 64-dim boxes (128-byte swizzle) and one
   // 32-dim box (64-byte swizzle), the layout the tensor core reads; fp8
@@ -191,11 +203,14 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
-int mla_uv_project(const void* attn_out, const void* w_uv, void* y, int batch, int num_heads, void* stream) {
+int mla_uv_project(const void* attn_out, const void* w_uv, void* y, int batch, int num_heads, void* workspace,
+                   void* stream) {
   if (batch < 0 || num_heads <= 0) return MLA_ERR_ARG;
   if (batch == 0) return MLA_OK;
   if (!attn_out || !w_uv || !y || !aligned(attn_out, 16) || !aligned(w_uv, 16) || !aligned(y, 16))
     return MLA_ERR_ARG;
+  if (workspace && !aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
+  int* status = workspace ? &reinterpret_cast<WsHeader*>(workspace)->status : nullptr;
   auto fn = encode_fn();
   if (!fn) return MLA_ERR_CUDA;
   CUtensorMap a_map, w_map;
@@ -213,7 +228,8 @@ int mla_uv_project(const void* attn_out, const void* w_uv, void* y, int batch, i
   if (!make_map_2d(&w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_uv, static_cast<uint64_t>(num_heads) * mla::kDimCkv,
                    mla::kDimV, mla::kDimV * 2, 64, 64))
     return MLA_ERR_CUDA;
-  cudaError_t e = mla::launch_uv_project(a_map, w_map, y, batch, num_heads, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      mla::launch_uv_project(a_map, w_map, y, batch, num_heads, status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -221,8 +237,12 @@ int mla_decode_noalloc(const mla_kv_pool* pool, int layer, const void* q, const 
                        const int32_t* page_ids, int max_blocks, const int32_t* context_lens, int batch,
                        int num_heads, float softmax_scale, int window, int num_clusters, void* out, float* lse,
                        int32_t* status, void* stream) {
-  if (!valid_pool(pool) || batch < 0 || window < 0 || num_clusters < 0) return MLA_ERR_ARG;
-  if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
+  if (num_clusters < 0) return MLA_ERR_ARG;
+  // Every argument check runs before the scratch is touched: a rejected call
+  // leaves the schedule of an earlier call that has not run yet intact.
+  const int rc0 = check_decode_args(pool, layer, q, page_indptr, page_ids, max_blocks, context_lens, batch,
+                                    num_heads, softmax_scale, window, out);
+  if (rc0 != MLA_OK) return rc0;
   const int cmax = max_clusters();
   if (cmax <= 0) return MLA_ERR_CUDA;
   const size_t need = mla::ws_layout(batch, num_heads, cmax).total;

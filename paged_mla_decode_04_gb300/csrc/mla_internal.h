@@ -101,6 +101,27 @@ struct DecodeArgs {
   float out_scale;   // 1, or kv_scale for fp8 pools (codes are dequantised by scaling O)
 };
 
+// Index of the current device for per-device caches (kMaxDevices entries),
+// or -1.
+constexpr int kMaxDevices = 64;
+inline int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+// Sets the dynamic shared memory limit of `kernel` once per device (the
+// attribute belongs to the device's context).
+template <typename K>
+inline cudaError_t set_smem_once(K kernel, int bytes, bool (&done)[kMaxDevices]) {
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (done[dev]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
 // Launch `kernel` on `stream` with programmatic stream serialization (see
 // pdl_wait in ptx.cuh): it may start while the previous kernel finishes.
 template <typename... KArgs, typename... Args>
@@ -135,6 +156,6 @@ cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& a, int clus
 int decode_max_active_clusters();
 // uv_project.cu
 cudaError_t launch_uv_project(const CUtensorMap& a_map, const CUtensorMap& w_map, void* y,
-                              int batch, int heads, cudaStream_t stream);
+                              int batch, int heads, int* status, cudaStream_t stream);
 
 }  // namespace mla

@@ -396,6 +396,15 @@ __device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t v) {
   return f2_make(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
+// f16 pair (low half first) to a packed fp32 pair, exactly.
+__device__ __forceinline__ uint64_t f2_from_f16x2(uint32_t v) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(v));
+  return f2_make(lo, hi);
+}
+
 // 32-byte vector store to global memory (one full sector).
 __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]),

@@ -27,7 +27,7 @@ constexpr int kThreads = 128;
 
 __global__ void __launch_bounds__(kThreads, 1)
     uv_project_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap w_map,
-                      __nv_bfloat16* __restrict__ y, int B, int H) {
+                      __nv_bfloat16* __restrict__ y, int B, int H, int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
@@ -59,6 +59,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the attention output is complete
 
+  // A wait that runs out in the producer or the issuer stops its loop: the
+  // accumulator's commit then never arrives and the epilogue's own bounded
+  // wait reports it.
   if (warp == 0 && lane == 0) {
     for (int kc = 0; kc < kKChunks; ++kc) {
       const int s = kc % kStages, use = kc / kStages;
@@ -83,16 +86,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16_ss(tmem, ad, bd, idesc, (kc | k) != 0);
       }
       mma_commit(empty(s));
+      if (kc == kKChunks - 1) mma_commit(done);
     }
-    mma_commit(done);
   }
   __syncwarp();
-  // Every thread waits for the accumulator (bounded), then reads its row.
+  // Every thread waits for the accumulator (bounded), then reads its row. If
+  // a wait ran out (the producer's, the issuer's or this one), the rows of
+  // this CTA are filled with NaN and the status word records the timeout, so
+  // y is never left silently stale.
   const bool ready = __all_sync(0xffffffffu, mbar_wait(done, 0, nullptr));
   tc_fence_after();
   const int row = warp * 32 + lane;
   const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  if (ready) {
+  if (!ready) {
+    if (status && threadIdx.x == 0) atomicOr(status, MLA_STATUS_TIMEOUT);
+    if (b0 + row < B) {
+      uint4* dst = reinterpret_cast<uint4*>(y + (static_cast<size_t>(b0 + row) * H + h) * kDimV);
+      const uint4 nan4 = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+#pragma unroll 1
+      for (int v = 0; v < kDimV * 2 / 16; ++v) dst[v] = nan4;
+    }
+  } else {
 #pragma unroll 1
     for (int c = 0; c < 128 / 32; ++c) {
       uint32_t r[32];
@@ -122,17 +136,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_uv_project(const CUtensorMap& a_map, const CUtensorMap& w_map, void* y, int batch,
-                              int heads, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(uv_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+                              int heads, int* status, cudaStream_t stream) {
+  static bool attr_set[kMaxDevices] = {};
+  const cudaError_t e = set_smem_once(uv_project_kernel, kSmemBytes, attr_set);
+  if (e != cudaSuccess) return e;
   const dim3 grid(heads, (batch + 127) / 128);
   return launch_pdl(uv_project_kernel, grid, dim3(kThreads), kSmemBytes, stream, a_map, w_map,
-                    static_cast<__nv_bfloat16*>(y), batch, heads);
+                    static_cast<__nv_bfloat16*>(y), batch, heads, status);
 }
 
 }  // namespace mla

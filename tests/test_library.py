@@ -47,7 +47,13 @@ def test_host_argument_checks_need_no_gpu(lib):
     lib.mla_get_error.restype = ctypes.c_int
     assert lib.mla_get_error(None, None, 0, None) == -1
     lib.mla_uv_project.restype = ctypes.c_int
-    assert lib.mla_uv_project(None, None, None, -1, 16, None) == -1
+    assert lib.mla_uv_project(None, None, None, -1, 16, None, None) == -1
+    assert lib.mla_uv_project(None, None, None, 4, 16, None, None) == -1
+    # a misaligned workspace for the status word is refused before any launch
+    buf = ctypes.create_string_buffer(1024)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    assert lib.mla_uv_project(ctypes.c_void_p(base), ctypes.c_void_p(base), ctypes.c_void_p(base), 4, 16,
+                              ctypes.c_void_p(base + 8), None) == -3
 
 
 def test_product_package_does_not_touch_the_oracle():

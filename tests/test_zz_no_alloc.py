@@ -56,3 +56,30 @@ def test_noalloc_rejects_calls_beyond_its_scratch():
                                 dw.lens.data_ptr(), too_many, 128, ctypes.c_float(0.07), 0, 0,
                                 dw.out.data_ptr(), None, None, 0)
     assert rc == -3                       # MLA_ERR_WORKSPACE, nothing launched
+
+
+def test_noalloc_rejected_call_leaves_the_previous_call_intact():
+    """A call with a bad argument (here a layer out of range) is refused before
+    it touches the shared scratch: an earlier call still in flight on the same
+    stream finishes with its own schedule and result."""
+    import paged_mla_decode_04_gb300 as m
+    lib = m.load_library()
+    wl = mw.make("v3", num_heads=128, context_lens=[3000, 17, 900])
+    dw = DeviceWorkload(wl, m)
+    ref_out, ref_lse = dw.step()
+    stream = torch.cuda.current_stream().cuda_stream
+    pool = dw.pool._c()
+    out = torch.full_like(dw.out, float("nan"))
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    args = (dw.q.data_ptr(), None, dw.block_table.data_ptr(), dw.block_table.shape[1],
+            dw.lens.data_ptr(), wl.batch, wl.num_heads, ctypes.c_float(wl.softmax_scale), wl.window, 0)
+    rc = lib.mla_decode_noalloc(ctypes.byref(pool), wl.layer, *args, out.data_ptr(), None,
+                                status.data_ptr(), stream)
+    assert rc == 0
+    bad_out = torch.empty_like(dw.out)
+    rc = lib.mla_decode_noalloc(ctypes.byref(pool), wl.num_layers, *args, bad_out.data_ptr(), None,
+                                None, stream)
+    assert rc == -1                       # MLA_ERR_ARG, nothing enqueued
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(f64(out), ref_out)
