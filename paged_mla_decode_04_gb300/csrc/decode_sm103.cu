@@ -129,6 +129,7 @@ struct Params {
   CUtensorMap kv_narrow;  // same rows: bf16 box {32, rows} 64B swizzle; fp8 box {32, rows}
   CUtensorMap q_wide;     // q rows [B*H][576] bf16, box {64, 128}, 128B swizzle
   CUtensorMap q_narrow;   // box {32, 128}, 64B swizzle
+  CUtensorMap kv_chunks;  // bf16 pools, page size >= 64: pool as [chunk 0-7][row][64 dims], box {64, 64, 4}
   DecodeArgs a;
 };
 
@@ -176,7 +177,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   const int cluster_id = blockIdx.x >> 1;
   const int H = a.num_heads;
   const int ps = a.page_size;
-  if (threadIdx.x == 0) MLA_TRACE_EVENT(5, kEvKernelStart, 0);
+  MLA_TRACER(trc5);  // kernel-level events (thread 0)
+  MLA_TRACER(trc);   // this thread's role events
+  if (threadIdx.x == 0) MLA_TRACE_EVENT(trc5, 5, kEvKernelStart, 0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -215,6 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     tma_prefetch_map(&p.kv_narrow);
     tma_prefetch_map(&p.q_wide);
     tma_prefetch_map(&p.q_narrow);
+    if (!kFp8 && ps >= kTile) tma_prefetch_map(&p.kv_chunks);
   }
   tc_fence_before();
   cluster_sync();  // barriers of both ranks initialised before any remote access
@@ -231,7 +235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     it_end = cstart[cluster_id + 1];
   }
   if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, MLA_STATUS_PLAN_MISMATCH);
-  if (threadIdx.x == 0) MLA_TRACE_EVENT(5, kEvSetupDone, it_end - it_begin);
+  if (threadIdx.x == 0) MLA_TRACE_EVENT(trc5, 5, kEvSetupDone, it_end - it_begin);
   const int wide_x = 256 * static_cast<int>(rank);        // first c_kv dim of this rank
   const int narrow_x = 512 + 32 * static_cast<int>(rank);  // first rope dim of this rank
 
@@ -342,7 +346,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         ++sl;
         if (!ok) break;
         if (lane == 0) {
-          MLA_TRACE_EVENT(0, kEvSlotAcquired, gt);
+          MLA_TRACE_EVENT(trc, 0, kEvSlotAcquired, gt);
           mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(nbox * rows_per_box) * row_bytes);
 #pragma unroll
           for (int bx = 0; bx < 4; ++bx) {
@@ -351,6 +355,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
               tma_load_2d_hint(dst0 + bx * rows_per_box * 256, &p.kv_wide, full_bar, wide_x, rows[bx], kv_policy);
               tma_load_2d_hint(dst0 + kF8WideBytes + bx * rows_per_box * 32, &p.kv_narrow, full_bar, narrow_x,
                                rows[bx], kv_policy);
+            } else if (rows_per_box == kTile) {
+              // one copy for this rank's four 64-dim chunks, chunk-major as the MMAs read them
+              tma_load_3d_hint(dst0, &p.kv_chunks, full_bar, 0, rows[bx], 4 * static_cast<int>(rank), kv_policy);
+              tma_load_2d_hint(dst0 + kWideChunks * kWideBytes, &p.kv_narrow, full_bar, narrow_x, rows[bx],
+                               kv_policy);
             } else {
               for (int c = 0; c < kWideChunks; ++c)
                 tma_load_2d_hint(dst0 + c * kWideBytes + bx * rows_per_box * 128, &p.kv_wide, full_bar,
@@ -359,7 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
                                narrow_x, rows[bx], kv_policy);
             }
           }
-          MLA_TRACE_EVENT(0, kEvTileIssued, gt);
+          MLA_TRACE_EVENT(trc, 0, kEvTileIssued, gt);
         }
         ++gt;
       }
@@ -421,14 +430,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         mma_commit(bar(kBarKvEmpty + s0));
         mma_commit(bar(kBarKvEmpty + s1));
         mma_commit(bar(kBarQnFree));
-        MLA_TRACE_EVENT(1, kEvQLoaded, g);
+        MLA_TRACE_EVENT(trc, 1, kEvQLoaded, g);
         sl += 2;
         for (int t = 0; t < nt; ++t, ++g, ++sl) {
           const uint32_t stage = sl % kStages, use = sl / kStages;
           if (!mbar_wait(bar(kBarKvFull + stage), use & 1u, abort_flag)) { ok = false; break; }
-          MLA_TRACE_EVENT(1, kEvQkTileReady, g);
+          MLA_TRACE_EVENT(trc, 1, kEvQkTileReady, g);
           if (!mbar_wait(bar(kBarSFree), (g & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-          MLA_TRACE_EVENT(1, kEvQkSFree, g);
+          MLA_TRACE_EVENT(trc, 1, kEvQkSFree, g);
           tc_fence_after();
           const uint32_t kv = sbase + kOffKV + stage * kStageBytes;
           // Descriptors of the tile's first chunk; the others differ only in
@@ -445,7 +454,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           for (int k = 0; k < 2; ++k)
             mma_bf16_ts(tS, tQ + 128u + 8u * k, dn + static_cast<uint64_t>((k * 32) >> 4), idesc_qk, 1u);
           mma_commit(bar(kBarSFull));
-          MLA_TRACE_EVENT(1, kEvQkIssued, g);
+          MLA_TRACE_EVENT(trc, 1, kEvQkIssued, g);
         }
         if (ok) mma_commit(bar(kBarQDone));  // every QK of this item complete: q may be replaced
       }
@@ -470,7 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         sl += 2;
         for (int t = 0; t < nt; ++t, ++g, ++sl) {
           if (!mbar_wait(bar(kBarOFixed), g & 1u, abort_flag)) { ok = false; break; }
-          MLA_TRACE_EVENT(2, kEvPvOFixed, g);
+          MLA_TRACE_EVENT(trc, 2, kEvPvOFixed, g);
           tc_fence_after();
           fence_proxy_async_smem();
           const uint64_t dv = sdesc_sw128(sbase + kOffKV + (sl % kStages) * kStageBytes, kWideBytes, 1024);
@@ -480,7 +489,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
                         (t | k) != 0);
           mma_commit(bar(kBarKvEmpty + sl % kStages));
           mma_commit(bar(kBarPvDone));
-          MLA_TRACE_EVENT(2, kEvPvIssued, g);
+          MLA_TRACE_EVENT(trc, 2, kEvPvIssued, g);
         }
       }
       if (!ok) {
@@ -614,7 +623,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     constexpr int kHalf = kTile / 2;
     const bool tracer = lane == 0 && (warp == C::kSmWarp0 || warp == C::kSmWarp0 + 7);
     auto tr = [&](uint32_t ev, uint32_t t) {
-      if (tracer) MLA_TRACE_EVENT(warp == C::kSmWarp0 ? 3 : 4, ev, t);
+      if (tracer) MLA_TRACE_EVENT(trc, warp == C::kSmWarp0 ? 3 : 4, ev, t);
     };
     auto wwait = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(b, parity, abort_flag));
@@ -696,9 +705,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         tmem_ld_h16<kHalf>(tmem + lane_base + kColS, r);
         tmem_ld_h16<kHalf>(tmem + lane_base + kColS + 16, r + 16);
         tmem_wait_ld();
+        const uint64_t sc2 = f2_make(a.scale_log2, a.scale_log2);
 #pragma unroll
-        for (int i = 0; i < kHalf / 2; ++i)
-          xp[i] = pack_f16x2(__uint_as_float(r[2 * i]) * a.scale_log2, __uint_as_float(r[2 * i + 1]) * a.scale_log2);
+        for (int i = 0; i < kHalf / 2; ++i) {
+          float s0, s1;
+          f2_split(f2_mul(f2_make(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2), s0, s1);
+          xp[i] = pack_f16x2(s0, s1);
+        }
       }
       tc_fence_before();
       mbar_arrive(bar(kBarSFree));
@@ -752,7 +765,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           // Scores as packed fp32 pairs (tokens 2i, 2i+1): both ranks add the
           // same two bf16 partials.
           uint64_t s2[kHalf / 2];
-          float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+          float mxa = -CUDART_INF_F, mxb = -CUDART_INF_F;
           if (valid) {
 #pragma unroll
             for (int j = 0; j < kHalf / 8; ++j) {
@@ -777,16 +790,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
               }
             }
 #pragma unroll
-            for (int i = 0; i < kHalf / 2; ++i) {
-              float s0, s1;
+            for (int i = 0; i < kHalf / 2; i += 2) {
+              float s0, s1, s2_, s3_;
               f2_split(s2[i], s0, s1);
-              mx4[(2 * i) & 3] = fmaxf(mx4[(2 * i) & 3], s0);
-              mx4[(2 * i + 1) & 3] = fmaxf(mx4[(2 * i + 1) & 3], s1);
+              f2_split(s2[i + 1], s2_, s3_);
+              mxa = fmax3(mxa, s0, s1);
+              mxb = fmax3(mxb, s2_, s3_);
             }
           }
           // The row max over both token halves (the partials were scaled to
           // log2 units before the exchange).
-          float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          float mx = fmaxf(mxa, mxb);
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           if (valid) {
             if (mx > m + kRescaleThreshold) {
@@ -871,7 +885,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     setmaxnreg_dec<C::kRegsIssue>();
   }
 
-  if (threadIdx.x == 0) MLA_TRACE_EVENT(5, kEvKernelEnd, 0);
+  if (threadIdx.x == 0) MLA_TRACE_EVENT(trc5, 5, kEvKernelEnd, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -916,6 +930,7 @@ cudaError_t launch_variant(const CUtensorMap* maps, const DecodeArgs& a, int clu
   p.kv_narrow = maps[1];
   p.q_wide = maps[2];
   p.q_narrow = maps[3];
+  p.kv_chunks = maps[4];
   p.a = a;
   return launch_pdl(mla_decode_kernel<kFp8>, dim3(2 * clusters), dim3(C::kThreads), C::kSmemBytes, stream, p);
 }

@@ -46,6 +46,21 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view of a bf16 pool for one copy of a rank's four 64-dim chunks: dims
+// {64 dims, rows, 8 chunks}, strides {row pitch, 128 bytes}, box {64, 64, 4}
+// (written to shared memory chunk-major, 128-byte swizzled).
+bool make_chunk_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, rows, 8};
+  cuuint64_t strides[2] = {mla::kDimRow * 2ull, 128};
+  cuuint32_t box[3] = {64, 64, 4};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool valid_pool(const mla_kv_pool* pool) {
@@ -152,7 +167,8 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   // 32-dim box (64-byte swizzle), the layout the tensor core reads; fp8
   // pools as one 256-byte and one 32-byte box, unswizzled, which the kernel
   // widens to f16 in that same layout.
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
+  memset(maps, 0, sizeof maps);
   const uint32_t box_rows = ps < mla::kBlockTokens ? ps : mla::kBlockTokens;
   const uint64_t q_rows = static_cast<uint64_t>(batch) * num_heads;
   const bool fp8 = pool->dtype == MLA_DTYPE_FP8_E4M3;
@@ -171,6 +187,7 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
       !make_map_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, q_rows, mla::kDimRow, mla::kDimRow * 2, 32,
                    128, CU_TENSOR_MAP_SWIZZLE_64B))
     return MLA_ERR_CUDA;
+  if (!fp8 && ps >= mla::kBlockTokens && !make_chunk_map(&maps[4], pool->data, total_rows)) return MLA_ERR_CUDA;
 
   mla::DecodeArgs a;
   memset(&a, 0, sizeof a);

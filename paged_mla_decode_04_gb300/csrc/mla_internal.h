@@ -151,7 +151,7 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int heads, int p
 cudaError_t launch_merge(const DecodeArgs& a, int clusters, cudaStream_t stream);
 // decode_sm103.cu
 // maps: {kv 64-dim boxes (128B swizzle), kv 32-dim boxes (64B swizzle),
-//        q 64-dim boxes, q 32-dim boxes}
+//        q 64-dim boxes, q 32-dim boxes, kv four-chunk boxes (bf16, page size >= 64)}
 cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& a, int clusters, cudaStream_t stream);
 int decode_max_active_clusters();
 // uv_project.cu

@@ -1,8 +1,9 @@
 // Optional event trace of the decode kernel's roles, compiled in only when
 // the library is built with -DMLA_TRACE (the default build has none of it).
 // Each role of each CTA appends records (SM clock, event, tile) to its own
-// slice of a device buffer; mla_trace_read copies the buffer to the host and
-// clears it. One writer per slice (lane 0 of the role's warp), so no atomics.
+// slice of a device buffer through its own Tracer; mla_trace_read copies the
+// buffer to the host and clears it. One writer per slice (lane 0 of the
+// role's warp), so no atomics.
 #pragma once
 
 #include <stdint.h>
@@ -29,6 +30,8 @@ enum TraceEvent : uint32_t {
   kEvPvOFixed,          // PV issuer: P of tile g ready
   kEvPvIssued,          // PV issuer: PV of tile g issued
   kEvQLoaded,           // QK issuer: q of the item ending before tile g copied to TMEM
+  kEvSmXRead,           // softmax: the peer's partials of tile g read and released
+  kEvSmPair,            // softmax: the row max of tile g shared with the row's other warp
 };
 
 constexpr int kTraceRoles = 6;     // producer, QK, PV, softmax (first warp), softmax (last warp), spare
@@ -42,18 +45,24 @@ namespace mla {
 __device__ uint64_t g_trace[kTraceCtas][kTraceRoles][kTraceCap];
 __device__ uint32_t g_trace_n[kTraceCtas][kTraceRoles];
 
-// Record: bits 0-39 SM clock, 40-47 event, 48-63 tile.
-__device__ __forceinline__ void trace_event(int role, uint32_t ev, uint32_t tile) {
-  const uint32_t cta = blockIdx.x;
-  if (cta >= kTraceCtas) return;
-  const uint32_t n = g_trace_n[cta][role];
-  if (n >= kTraceCap) return;
-  g_trace[cta][role][n] =
-      (clock64() & 0xFFFFFFFFFFull) | (static_cast<uint64_t>(ev & 0xFF) << 40) | (static_cast<uint64_t>(tile & 0xFFFF) << 48);
-  g_trace_n[cta][role] = n + 1;
-}
+// One role's writer. Record: bits 0-39 SM clock, 40-47 event, 48-63 tile.
+// The count lives in a register and is published with every record (a
+// store only: reading it back from global memory would put an L2 round trip
+// on every event).
+struct Tracer {
+  uint32_t n = 0;
+  __device__ __forceinline__ void operator()(int role, uint32_t ev, uint32_t tile) {
+    const uint32_t cta = blockIdx.x;
+    if (cta >= kTraceCtas || n >= kTraceCap) return;
+    g_trace[cta][role][n] = (clock64() & 0xFFFFFFFFFFull) | (static_cast<uint64_t>(ev & 0xFF) << 40) |
+                            (static_cast<uint64_t>(tile & 0xFFFF) << 48);
+    g_trace_n[cta][role] = ++n;
+  }
+};
 }  // namespace mla
-#define MLA_TRACE_EVENT(role, ev, tile) ::mla::trace_event((role), (ev), (tile))
+#define MLA_TRACER(name) ::mla::Tracer name
+#define MLA_TRACE_EVENT(tracer, role, ev, tile) (tracer)((role), (ev), (tile))
 #else
-#define MLA_TRACE_EVENT(role, ev, tile) ((void)0)
+#define MLA_TRACER(name) struct {} name
+#define MLA_TRACE_EVENT(tracer, role, ev, tile) ((void)0)
 #endif
