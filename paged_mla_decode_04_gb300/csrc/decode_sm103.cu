@@ -642,7 +642,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     const uint32_t peer_xfull0 = mapa(xfull(0), peer), peer_xfull1 = mapa(xfull(1), peer);
     const uint32_t peer_xfree0 = mapa(xfree(0), peer), peer_xfree1 = mapa(xfree(1), peer);
     // Epilogue of an item: wait for its last PV, normalise this thread's
-    // 128 value dims, store.
+    // 128 value dims, store. TMEM is read several 16-column chunks per wait.
     auto store_item = [&](const WorkItem& w, uint32_t g_last, float m, float l) -> bool {
       tr(kEvSmItemStore, g_last);
       if (!wwait(bar(kBarPvDone), g_last & 1u)) return false;
@@ -657,28 +657,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       }
       if (nrow > 0) {
         const float inv_l = valid ? a.out_scale / l : 0.f;  // out_scale: kv_scale for fp8 pools
+        constexpr int kBatch = kFp8 ? 2 : 4;  // 16-column chunks per TMEM wait (registers)
 #pragma unroll 1
-        for (int c = 0; c < 128 / 16; ++c) {
-          uint32_t o[16];
-          tmem_ld_h16<128>(tO + c * 16, o);
+        for (int c0 = 0; c0 < 128 / 16; c0 += kBatch) {
+          uint32_t o[kBatch][16];
+#pragma unroll
+          for (int c = 0; c < kBatch; ++c) tmem_ld_h16<128>(tO + (c0 + c) * 16, o[c]);
           tmem_wait_ld();
           if (valid) {
-            // Whole 32-byte sectors per store (16 bf16 or 8 fp32 dims).
-            if (w.slot < 0) {
-              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                                   (static_cast<size_t>(w.b) * H + row) * kDimCkv + dim0 + c * 16;
-              uint32_t pk[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-              st_global_v8(dst, pk);
-            } else {
-              float* dst = reinterpret_cast<float*>(ws + a.lay.partial_o) +
-                           (static_cast<size_t>(w.slot) * H + row) * kDimCkv + dim0 + c * 16;
+            for (int c = 0; c < kBatch; ++c) {
+              // Whole 32-byte sectors per store (16 bf16 or 8 fp32 dims).
+              if (w.slot < 0) {
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
+                                     (static_cast<size_t>(w.b) * H + row) * kDimCkv + dim0 + (c0 + c) * 16;
+                uint32_t pk[8];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv_l);
-              st_global_v8(dst, o);
-              st_global_v8(dst + 8, o + 8);
+                for (int i = 0; i < 8; ++i)
+                  pk[i] = pack_bf16x2(__uint_as_float(o[c][2 * i]) * inv_l, __uint_as_float(o[c][2 * i + 1]) * inv_l);
+                st_global_v8(dst, pk);
+              } else {
+                float* dst = reinterpret_cast<float*>(ws + a.lay.partial_o) +
+                             (static_cast<size_t>(w.slot) * H + row) * kDimCkv + dim0 + (c0 + c) * 16;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[c][i] = __float_as_uint(__uint_as_float(o[c][i]) * inv_l);
+                st_global_v8(dst, o[c]);
+                st_global_v8(dst + 8, o[c] + 8);
+              }
             }
           }
         }
