@@ -159,6 +159,36 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q,
                int num_heads, float softmax_scale, int window,
                void* workspace, void* out, float* lse, void* stream);
 
+/* Several query positions per request: multi-token decode (speculative or
+ * multi-token-prediction steps, LightLLM PR #1593 "Support dsv4 model",
+ * Summary and Validation) and, with longer runs of positions, the absorbed
+ * form of chunked prefill over the paged latent (vLLM #12639 "[Attention]
+ * MLA with chunked prefill", Future work). Request b holds L_b =
+ * context_lens[b] cached tokens before this step; its q_len new tokens sit
+ * at positions L_b .. L_b + q_len - 1 (their latent rows written beforehand
+ * with mla_kv_write, q_len slots per request), and query position i attends
+ * positions [start_i, L_b + i] with start_i = 0, or max(0, L_b + i + 1 -
+ * window): causal within the step. q_len = 1 is mla_decode exactly.
+ *   q:   device [batch][q_len][num_heads][576] bf16, 16-byte aligned.
+ *   out: device [batch][q_len][num_heads][512] bf16, 32-byte aligned;
+ *   lse: device [batch][q_len][num_heads] fp32 or NULL.
+ * The q_len x num_heads rows of a request run in groups of 128 (one
+ * tensor-core tile of rows); each group reads the request's pages once.
+ * batch x q_len x num_heads must stay below 2^31 (MLA_ERR_ARG).
+ * Workspace and plan: mla_decode_workspace_size_q and mla_decode_plan_q with
+ * the same batch, q_len and num_heads (a plan made for another q_len sets
+ * MLA_STATUS_PLAN_MISMATCH). Everything else as for mla_decode. */
+size_t mla_decode_workspace_size_q(int batch, int q_len, int num_heads);
+int mla_decode_plan_q(const int32_t* context_lens, int batch, int q_len,
+                      int num_heads, int page_size, int window,
+                      int num_clusters, void* workspace,
+                      size_t workspace_bytes, void* stream);
+int mla_decode_q(const mla_kv_pool* pool, int layer, const void* q,
+                 const int32_t* page_indptr, const int32_t* page_ids,
+                 int max_blocks, const int32_t* context_lens, int batch,
+                 int q_len, int num_heads, float softmax_scale, int window,
+                 void* workspace, void* out, float* lse, void* stream);
+
 /* W_UV projection after attention: y[b,h,:] = attn_out[b,h,:] @ w_uv[h],
  * v_head_dim 128 (MoE-Infinity PR #195, Root causes 3).
  *   attn_out: device [batch][num_heads][512] bf16; w_uv: device

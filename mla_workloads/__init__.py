@@ -65,14 +65,17 @@ class Workload:
     softmax_scale: float = 192.0 ** -0.5
     w_uv: Optional[np.ndarray] = None   # uint16 bf16 bits [H, 512, 128]
     extra: dict = field(default_factory=dict)
+    q_len: int = 1                  # query positions per request (q is [B, q_len, H, 576] if > 1)
 
     @property
     def attended(self) -> np.ndarray:
-        """Tokens each request attends (new token included)."""
+        """Tokens each request attends over all its query positions (new
+        tokens included)."""
         L = self.context_lens.astype(np.int64)
+        end = L + self.q_len
         if self.window > 0:
-            return np.minimum(L + 1, self.window)
-        return L + 1
+            return end - np.maximum(0, L + 1 - self.window)
+        return end
 
     @property
     def row_bytes(self) -> int:
@@ -136,10 +139,12 @@ def make(name: str, seed: Optional[int] = None, batch: Optional[int] = None,
          num_heads: Optional[int] = None, context_lens=None, page_size: Optional[int] = None,
          window: Optional[int] = None, num_layers: int = 2, layer: int = 1,
          spare_pages: int = SPARE_PAGES, value_std: Optional[float] = None,
-         q_std: float = 1.0) -> Workload:
+         q_std: float = 1.0, q_len: int = 1) -> Workload:
     """Build one seeded workload. Overrides shrink a configuration for tests;
     value_std and q_std change the spread of the cache values and of q (for
-    score scales like a trained model's, where the softmax is peaked)."""
+    score scales like a trained model's, where the softmax is peaked). q_len >
+    1 gives each request q_len new tokens at positions L .. L + q_len - 1
+    (q [B, q_len, H, 576], new_rows and slot_mapping [B * q_len])."""
     B0, H0, ps0, dtype, W0, std, has_uv = CONFIGS[name]
     std = std if value_std is None else value_std
     seed = SEEDS[name] if seed is None else seed
@@ -153,7 +158,7 @@ def make(name: str, seed: Optional[int] = None, batch: Optional[int] = None,
     else:
         B = B0 if batch is None else batch
         L = _lengths(name, rng, B)
-    n_blocks = (L.astype(np.int64) // ps) + 1          # blocks holding positions 0..L
+    n_blocks = ((L.astype(np.int64) + q_len - 1) // ps) + 1   # blocks holding positions 0..L+q_len-1
     P = int(n_blocks.sum()) + spare_pages
     perm = rng.permutation(P).astype(np.int32)
     max_blocks = int(n_blocks.max()) if B else 1
@@ -164,10 +169,10 @@ def make(name: str, seed: Optional[int] = None, batch: Optional[int] = None,
     for b in range(B):
         block_table[b, : n_blocks[b]] = ids[indptr[b]: indptr[b + 1]]
     pool = _normal_bf16(rng, (num_layers, P, ps, D_ROW), std)
-    q = _normal_bf16(rng, (B, H, D_ROW), q_std)
-    new_rows = _normal_bf16(rng, (B, D_ROW), std)
-    slots = np.array([int(block_table[b, L[b] // ps]) * ps + int(L[b]) % ps for b in range(B)],
-                     np.int64)
+    q = _normal_bf16(rng, (B, H, D_ROW) if q_len == 1 else (B, q_len, H, D_ROW), q_std)
+    new_rows = _normal_bf16(rng, (B * q_len, D_ROW), std)
+    slots = np.array([int(block_table[b, (L[b] + i) // ps]) * ps + (int(L[b]) + i) % ps
+                      for b in range(B) for i in range(q_len)], np.int64)
     kv_scale = 1.0
     if dtype == FP8_E4M3:
         amax = max(float(np.abs(bf16_bits_to_f32(pool)).max()),
@@ -178,7 +183,7 @@ def make(name: str, seed: Optional[int] = None, batch: Optional[int] = None,
                   context_lens=L, window=W, num_layers=num_layers, layer=layer,
                   num_pages=P, block_table=block_table, page_indptr=indptr, page_ids=ids,
                   pool_bf16=pool, kv_scale=kv_scale, q=q, new_rows=new_rows,
-                  slot_mapping=slots, w_uv=w_uv)
+                  slot_mapping=slots, w_uv=w_uv, q_len=q_len)
     if name == "tiny":
         # Unabsorbed-form parameters: q_nope, q_rope ~ N(0,1); W_UK ~ N(0, 1/128)
         # so that W_UK^T q_nope has unit variance; W_UV ~ N(0, 0.02^2).

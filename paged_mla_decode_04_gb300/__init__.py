@@ -10,6 +10,8 @@ Calls (same names as the C ABI in include/mla_decode.h):
   plan(context_lens, num_heads, page_size, window, workspace, num_clusters=0)
   decode(pool, layer, q, context_lens, softmax_scale, workspace, out,
          block_table=None | page_indptr + page_ids, window=0, lse=None)
+  workspace_size_q / plan_q / decode_q: several query positions per request
+  (q [batch, q_len, heads, 576]; causal within the step)
   uv_project(attn_out, w_uv, y, workspace=None)
   get_error(workspace, clear=False)
 """
@@ -40,7 +42,8 @@ V_HEAD_DIM = 128
 
 EXPORTED = ["mla_kv_write", "mla_decode_workspace_size", "mla_decode_num_clusters",
             "mla_decode_plan", "mla_decode", "mla_uv_project", "mla_get_error",
-            "mla_decode_noalloc"]
+            "mla_decode_noalloc", "mla_decode_workspace_size_q", "mla_decode_plan_q",
+            "mla_decode_q"]
 NOALLOC_SCRATCH_BYTES = 48 << 20
 
 
@@ -84,6 +87,13 @@ def load_library(path: str = LIB_PATH):
     lib.mla_decode_noalloc.argtypes = [ctypes.POINTER(_Pool), I, P, P, P, I, P, I, I, ctypes.c_float,
                                        I, I, P, P, P, P]
     lib.mla_decode_noalloc.restype = I
+    lib.mla_decode_workspace_size_q.argtypes = [I, I, I]
+    lib.mla_decode_workspace_size_q.restype = Z
+    lib.mla_decode_plan_q.argtypes = [P, I, I, I, I, I, I, P, Z, P]
+    lib.mla_decode_plan_q.restype = I
+    lib.mla_decode_q.argtypes = [ctypes.POINTER(_Pool), I, P, P, P, I, P, I, I, I, ctypes.c_float, I,
+                                 P, P, P, P]
+    lib.mla_decode_q.restype = I
     _lib = lib
     return lib
 
@@ -250,3 +260,63 @@ def get_error(workspace: torch.Tensor, clear: bool = False, stream=None) -> int:
                                       1 if clear else 0, _stream(stream))
     _check(rc, "mla_get_error")
     return code.value
+
+
+# ----------------------------------------------------------------- several query positions per request
+
+def workspace_size_q(batch: int, q_len: int, num_heads: int) -> int:
+    n = load_library().mla_decode_workspace_size_q(batch, q_len, num_heads)
+    if n == 0:
+        raise MlaError("mla_decode_workspace_size_q: unsupported arguments")
+    return n
+
+
+def alloc_workspace_q(batch: int, q_len: int, num_heads: int, device=None) -> torch.Tensor:
+    return torch.zeros(workspace_size_q(batch, q_len, num_heads), dtype=torch.uint8,
+                       device=device or torch.device("cuda"))
+
+
+def plan_q(context_lens: torch.Tensor, q_len: int, num_heads: int, page_size: int, window: int,
+           workspace: torch.Tensor, num_clusters: int = 0, stream=None) -> None:
+    lib = load_library()
+    rc = lib.mla_decode_plan_q(_dev(context_lens, "context_lens", torch.int32), context_lens.numel(), q_len,
+                               num_heads, page_size, window, num_clusters, _dev(workspace, "workspace"),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "mla_decode_plan_q")
+
+
+def decode_q(pool: KVPool, layer: int, q: torch.Tensor, context_lens: torch.Tensor,
+             softmax_scale: float, workspace: torch.Tensor, out: torch.Tensor,
+             block_table: Optional[torch.Tensor] = None, page_indptr: Optional[torch.Tensor] = None,
+             page_ids: Optional[torch.Tensor] = None, window: int = 0,
+             lse: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """q [batch, q_len, heads, 576] -> out [batch, q_len, heads, 512] (lse
+    [batch, q_len, heads]); query position i of request b attends positions
+    up to context_lens[b] + i."""
+    lib = load_library()
+    if q.dim() != 4 or q.shape[3] != LATENT_DIM:
+        raise ValueError("q must be [batch, q_len, heads, 576]")
+    B, QL, H, _ = q.shape
+    if out.shape != (B, QL, H, KV_LORA_RANK):
+        raise ValueError("out must be [batch, q_len, heads, 512]")
+    if lse is not None and lse.shape != (B, QL, H):
+        raise ValueError("lse must be [batch, q_len, heads]")
+    if block_table is not None:
+        if block_table.dim() != 2 or block_table.shape[0] != B:
+            raise ValueError("block_table must be [batch, max_blocks]")
+        indptr_p, ids_p, max_blocks = None, _dev(block_table, "block_table", torch.int32), \
+            block_table.shape[1]
+    else:
+        if page_indptr is None or page_ids is None or page_indptr.shape != (B + 1,):
+            raise ValueError("give block_table, or page_indptr [batch+1] and page_ids")
+        indptr_p = _dev(page_indptr, "page_indptr", torch.int32)
+        ids_p, max_blocks = _dev(page_ids, "page_ids", torch.int32), 0
+    if context_lens.shape != (B,):
+        raise ValueError("context_lens must be [batch]")
+    c = pool._c()
+    rc = lib.mla_decode_q(ctypes.byref(c), layer, _dev(q, "q", torch.bfloat16), indptr_p, ids_p, max_blocks,
+                          _dev(context_lens, "context_lens", torch.int32), B, QL, H, float(softmax_scale),
+                          window, _dev(workspace, "workspace"), _dev(out, "out", torch.bfloat16),
+                          None if lse is None else _dev(lse, "lse", torch.float32), _stream(stream))
+    _check(rc, "mla_decode_q")
+    return out

@@ -228,6 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   // workspace, the pool and q are read.
   pdl_wait();
   const bool plan_ok = hd->planned == 1 && hd->batch == a.batch && hd->num_heads == a.num_heads &&
+                       hd->q_len == a.q_len &&
                        hd->page_size == a.page_size && hd->window == a.window;
   int it_begin = 0, it_end = 0;
   if (plan_ok && cluster_id < hd->num_clusters) {
@@ -278,7 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           mbar_arrive_expect_tx(fb, 2 * kQWideBytes);
           for (int c = 0; c < 2; ++c)
             tma_load_2d(sbase + kOffKV + stage * kStageBytes + c * kQWideBytes, &p.q_wide, fb,
-                        wide_x + 64 * (2 * h + c), w.b * H);
+                        wide_x + 64 * (2 * h + c), w.b * a.rows + w.row0);
         }
         if (ok) {
           last_q_item = static_cast<int>(n_items);
@@ -291,7 +292,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       if (lane == 0) {
         const uint32_t qb = bar(kFp8 ? kBarQnRaw : kBarQnFull);
         mbar_arrive_expect_tx(qb, kQNarrowBytes);
-        tma_load_2d(sbase + kOffQn, &p.q_narrow, qb, narrow_x, w.b * H);
+        tma_load_2d(sbase + kOffQn, &p.q_narrow, qb, narrow_x, w.b * a.rows + w.row0);
       }
       last_qn_item = static_cast<int>(n_items);
       for (int blk = w.blk_begin; blk < w.blk_end; ++blk) {
@@ -615,7 +616,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     const int half = (warp - C::kSmWarp0) >> 2;     // lane half of the quarter
     const int th = lane >> 4;                       // token half of a tile / value-dim half
     const int row = 32 * q4 + 16 * half + (lane & 15);
-    const int nrow = min(max(H - 32 * q4 - 16 * half, 0), 16);  // valid heads of this warp
+    // rows of a row group in use (heads, or query positions x heads)
+    const int nrow = min(max(a.group_rows - 32 * q4 - 16 * half, 0), 16);  // valid rows of this warp
     const bool valid = (lane & 15) < nrow;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4 + 16 * half) << 16;
     const uint32_t tO = tmem + lane_base + kColO;   // this warp's 16 rows of O
@@ -643,20 +645,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     const uint32_t peer_xfree0 = mapa(xfree(0), peer), peer_xfree1 = mapa(xfree(1), peer);
     // Epilogue of an item: wait for its last PV, normalise this thread's
     // 128 value dims, store. TMEM is read several 16-column chunks per wait.
+    // A row with no attended token in an item (a query position whose range
+    // ends before a split item of a later one) has l = 0: its partial is 0
+    // with lse = -inf, which the merge weighs 0.
     auto store_item = [&](const WorkItem& w, uint32_t g_last, float m, float l) -> bool {
       tr(kEvSmItemStore, g_last);
       if (!wwait(bar(kBarPvDone), g_last & 1u)) return false;
       tc_fence_after();
-      if (rank == 0 && th == 0 && valid) {
-        const float lse2 = m + log2f(l);
+      const bool keep = valid && w.row0 + row < a.rows;  // rows past the request's last row are not stored
+      const size_t out_row = static_cast<size_t>(w.b) * a.rows + w.row0 + row;
+      const size_t part_row = static_cast<size_t>(w.slot) * a.group_rows + row;
+      if (rank == 0 && th == 0 && keep) {
+        const float lse2 = l > 0.f ? m + log2f(l) : -CUDART_INF_F;
         if (w.slot < 0) {
-          if (a.lse) a.lse[static_cast<size_t>(w.b) * H + row] = lse2 * 0.69314718055994531f;
+          if (a.lse) a.lse[out_row] = lse2 * 0.69314718055994531f;
         } else {
-          reinterpret_cast<float*>(ws + a.lay.partial_lse)[static_cast<size_t>(w.slot) * H + row] = lse2;
+          reinterpret_cast<float*>(ws + a.lay.partial_lse)[part_row] = lse2;
         }
       }
       if (nrow > 0) {
-        const float inv_l = valid ? a.out_scale / l : 0.f;  // out_scale: kv_scale for fp8 pools
+        const float inv_l = keep && l > 0.f ? a.out_scale / l : 0.f;  // out_scale: kv_scale for fp8 pools
         constexpr int kBatch = kFp8 ? 2 : 4;  // 16-column chunks per TMEM wait (registers)
 #pragma unroll 1
         for (int c0 = 0; c0 < 128 / 16; c0 += kBatch) {
@@ -664,21 +672,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
 #pragma unroll
           for (int c = 0; c < kBatch; ++c) tmem_ld_h16<128>(tO + (c0 + c) * 16, o[c]);
           tmem_wait_ld();
-          if (valid) {
+          if (keep) {
 #pragma unroll
             for (int c = 0; c < kBatch; ++c) {
               // Whole 32-byte sectors per store (16 bf16 or 8 fp32 dims).
               if (w.slot < 0) {
-                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                                     (static_cast<size_t>(w.b) * H + row) * kDimCkv + dim0 + (c0 + c) * 16;
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + out_row * kDimCkv + dim0 + (c0 + c) * 16;
                 uint32_t pk[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                   pk[i] = pack_bf16x2(__uint_as_float(o[c][2 * i]) * inv_l, __uint_as_float(o[c][2 * i + 1]) * inv_l);
                 st_global_v8(dst, pk);
               } else {
-                float* dst = reinterpret_cast<float*>(ws + a.lay.partial_o) +
-                             (static_cast<size_t>(w.slot) * H + row) * kDimCkv + dim0 + (c0 + c) * 16;
+                float* dst = reinterpret_cast<float*>(ws + a.lay.partial_o) + part_row * kDimCkv + dim0 + (c0 + c) * 16;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) o[c][i] = __float_as_uint(__uint_as_float(o[c][i]) * inv_l);
                 st_global_v8(dst, o[c]);
@@ -749,8 +755,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     }
     for (int it = it_begin; it < it_end && ok; ++it) {
       const WorkItem w = items[it];
+      // Positions of the item: [lo, hi) for all of its rows; this row (query
+      // position qi) attends [lo_r, hi_r) of them: positions up to L + qi.
       const int lo = max(w.blk_begin * kTile, w.tok_lo);
       const int hi = min(w.blk_end * kTile, w.tok_hi);
+      const int qi = (w.row0 + row) / H;
+      const int row_end = w.tok_hi - (a.q_len - 1 - qi);
+      const int hi_r = min(hi, row_end);
+      const int lo_r = a.window > 0 ? max(lo, row_end - a.window) : lo;
       float m = -CUDART_INF_F, l = 0.f;  // l: this thread's tokens only
       sl += 2;  // the item's q slots
       for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++g, ++sl) {
@@ -783,14 +795,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           __syncwarp();
           if (lane == 0) mbar_arrive_remote_relaxed(b ? peer_xfree1 : peer_xfree0);  // X[b] read
           if (valid) {
-            if (lo > base || hi < base + kHalf) {
+            if (lo_r > base || hi_r < base + kHalf) {
 #pragma unroll
               for (int i = 0; i < kHalf / 2; ++i) {
                 float s0, s1;
                 f2_split(s2[i], s0, s1);
                 const int pos = base + 2 * i;
-                if (pos < lo || pos >= hi) s0 = -CUDART_INF_F;
-                if (pos + 1 < lo || pos + 1 >= hi) s1 = -CUDART_INF_F;
+                if (pos < lo_r || pos >= hi_r) s0 = -CUDART_INF_F;
+                if (pos + 1 < lo_r || pos + 1 >= hi_r) s1 = -CUDART_INF_F;
                 s2[i] = f2_make(s0, s1);
               }
             }
@@ -813,7 +825,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
               l *= alpha;
               m = mx;
             }
-            const uint64_t nm2 = f2_make(-m, -m);
+            // (a row that has seen no attended token yet keeps m = -inf; its
+            // masked scores then give P = 0, not 2^(-inf + inf))
+            const float m_use = m == -CUDART_INF_F ? 0.f : m;
+            const uint64_t nm2 = f2_make(-m_use, -m_use);
             uint64_t rs2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) {

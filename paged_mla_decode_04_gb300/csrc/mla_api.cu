@@ -74,13 +74,22 @@ bool valid_pool(const mla_kv_pool* pool) {
 
 int max_clusters() { return mla::decode_max_active_clusters(); }
 
-// The host-visible checks of mla_decode (everything but the workspace), so
+bool valid_heads(int h) { return h == 16 || h == 32 || h == 64 || h == 128; }
+
+// Scheduled requests and rows per scheduled request of (batch, q_len,
+// heads): each request's q_len x heads rows in groups of at most 128.
+mla::WsLayout layout_of(int batch, int q_len, int heads, int clusters) {
+  return mla::ws_layout(batch * mla::row_groups(q_len, heads), mla::group_rows(q_len, heads), clusters);
+}
+
+// The host-visible checks of mla_decode_q (everything but the workspace), so
 // that mla_decode_noalloc can run them before it touches its scratch.
 int check_decode_args(const mla_kv_pool* pool, int layer, const void* q, const int32_t* page_indptr,
                       const int32_t* page_ids, int max_blocks, const int32_t* context_lens, int batch,
-                      int num_heads, float softmax_scale, int window, const void* out) {
+                      int q_len, int num_heads, float softmax_scale, int window, const void* out) {
   if (!valid_pool(pool) || layer < 0 || layer >= pool->num_layers || batch < 0 || window < 0) return MLA_ERR_ARG;
-  if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
+  if (!valid_heads(num_heads)) return MLA_ERR_UNSUPPORTED;
+  if (q_len < 1 || static_cast<int64_t>(batch) * q_len * num_heads >= (1ll << 31)) return MLA_ERR_ARG;
   if (batch == 0) return MLA_OK;
   if (!q || !page_ids || !context_lens || !out || !aligned(q, 16) || !aligned(out, 32)) return MLA_ERR_ARG;
   if (!page_indptr && max_blocks <= 0) return MLA_ERR_ARG;
@@ -126,6 +135,14 @@ int mla_decode_num_clusters(void) {
   return c > 0 ? c : MLA_ERR_CUDA;
 }
 
+size_t mla_decode_workspace_size_q(int batch, int q_len, int num_heads) {
+  if (batch < 0 || q_len < 1 || !valid_heads(num_heads)) return 0;
+  if (static_cast<int64_t>(batch) * q_len * num_heads >= (1ll << 31)) return 0;
+  const int c = max_clusters();
+  if (c <= 0) return 0;
+  return layout_of(batch, q_len, num_heads, c).total;
+}
+
 size_t mla_decode_workspace_size(int batch, int num_heads) {
   if (batch < 0 || num_heads <= 0 || num_heads > 128) return 0;
   const int c = max_clusters();
@@ -133,28 +150,36 @@ size_t mla_decode_workspace_size(int batch, int num_heads) {
   return mla::ws_layout(batch, num_heads, c).total;
 }
 
-int mla_decode_plan(const int32_t* context_lens, int batch, int num_heads, int page_size, int window,
-                    int num_clusters, void* workspace, size_t workspace_bytes, void* stream) {
-  if (batch < 0 || window < 0 || num_clusters < 0 || !workspace) return MLA_ERR_ARG;
+int mla_decode_plan_q(const int32_t* context_lens, int batch, int q_len, int num_heads, int page_size, int window,
+                      int num_clusters, void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch < 0 || q_len < 1 || window < 0 || num_clusters < 0 || !workspace) return MLA_ERR_ARG;
   if (batch > 0 && !context_lens) return MLA_ERR_ARG;
-  if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
+  if (!valid_heads(num_heads)) return MLA_ERR_UNSUPPORTED;
   if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(batch) * q_len * num_heads >= (1ll << 31)) return MLA_ERR_ARG;
   const int cmax = max_clusters();
   if (cmax <= 0) return MLA_ERR_CUDA;
-  const WsLayout lay = mla::ws_layout(batch, num_heads, cmax);
+  const WsLayout lay = layout_of(batch, q_len, num_heads, cmax);
   if (!aligned(workspace, 256) || workspace_bytes < lay.total) return MLA_ERR_WORKSPACE;
   const int c = (num_clusters == 0 || num_clusters > cmax) ? cmax : num_clusters;
-  cudaError_t e = mla::launch_plan(context_lens, batch, num_heads, page_size, window, c,
+  cudaError_t e = mla::launch_plan(context_lens, batch, q_len, num_heads, page_size, window, c,
                                    static_cast<uint8_t*>(workspace), lay, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
-int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t* page_indptr,
-               const int32_t* page_ids, int max_blocks, const int32_t* context_lens, int batch, int num_heads,
-               float softmax_scale, int window, void* workspace, void* out, float* lse, void* stream) {
+int mla_decode_plan(const int32_t* context_lens, int batch, int num_heads, int page_size, int window,
+                    int num_clusters, void* workspace, size_t workspace_bytes, void* stream) {
+  return mla_decode_plan_q(context_lens, batch, 1, num_heads, page_size, window, num_clusters, workspace,
+                           workspace_bytes, stream);
+}
+
+int mla_decode_q(const mla_kv_pool* pool, int layer, const void* q, const int32_t* page_indptr,
+                 const int32_t* page_ids, int max_blocks, const int32_t* context_lens, int batch, int q_len,
+                 int num_heads, float softmax_scale, int window, void* workspace, void* out, float* lse,
+                 void* stream) {
   if (!workspace) return MLA_ERR_ARG;
   const int rc = check_decode_args(pool, layer, q, page_indptr, page_ids, max_blocks, context_lens, batch,
-                                   num_heads, softmax_scale, window, out);
+                                   q_len, num_heads, softmax_scale, window, out);
   if (rc != MLA_OK || batch == 0) return rc;
   const int cmax = max_clusters();
   if (cmax <= 0) return MLA_ERR_CUDA;
@@ -170,7 +195,7 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   CUtensorMap maps[5];
   memset(maps, 0, sizeof maps);
   const uint32_t box_rows = ps < mla::kBlockTokens ? ps : mla::kBlockTokens;
-  const uint64_t q_rows = static_cast<uint64_t>(batch) * num_heads;
+  const uint64_t q_rows = static_cast<uint64_t>(batch) * q_len * num_heads;
   const bool fp8 = pool->dtype == MLA_DTYPE_FP8_E4M3;
   const bool kv_ok =
       fp8 ? make_map_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, pool->data, total_rows, mla::kDimRow, mla::kDimRow,
@@ -198,10 +223,14 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   a.out = out;
   a.lse = lse;
   a.ws = static_cast<uint8_t*>(workspace);
-  a.lay = mla::ws_layout(batch, num_heads, cmax);
+  a.lay = layout_of(batch, q_len, num_heads, cmax);
   a.max_blocks = max_blocks;
   a.batch = batch;
   a.num_heads = num_heads;
+  a.q_len = q_len;
+  a.rows = q_len * num_heads;
+  a.group_rows = mla::group_rows(q_len, num_heads);
+  a.groups = mla::row_groups(q_len, num_heads);
   a.page_size = ps;
   a.window = window;
   a.num_pages = pool->num_pages;
@@ -218,6 +247,13 @@ int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t*
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   e = mla::launch_merge(a, cmax, st);
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_decode(const mla_kv_pool* pool, int layer, const void* q, const int32_t* page_indptr,
+               const int32_t* page_ids, int max_blocks, const int32_t* context_lens, int batch, int num_heads,
+               float softmax_scale, int window, void* workspace, void* out, float* lse, void* stream) {
+  return mla_decode_q(pool, layer, q, page_indptr, page_ids, max_blocks, context_lens, batch, 1, num_heads,
+                      softmax_scale, window, workspace, out, lse, stream);
 }
 
 int mla_uv_project(const void* attn_out, const void* w_uv, void* y, int batch, int num_heads, void* workspace,
@@ -257,7 +293,7 @@ int mla_decode_noalloc(const mla_kv_pool* pool, int layer, const void* q, const 
   if (num_clusters < 0) return MLA_ERR_ARG;
   // Every argument check runs before the scratch is touched: a rejected call
   // leaves the schedule of an earlier call that has not run yet intact.
-  const int rc0 = check_decode_args(pool, layer, q, page_indptr, page_ids, max_blocks, context_lens, batch,
+  const int rc0 = check_decode_args(pool, layer, q, page_indptr, page_ids, max_blocks, context_lens, batch, 1,
                                     num_heads, softmax_scale, window, out);
   if (rc0 != MLA_OK) return rc0;
   const int cmax = max_clusters();

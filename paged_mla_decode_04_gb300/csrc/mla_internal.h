@@ -15,9 +15,26 @@ constexpr int kDimRope = 64;
 constexpr int kDimRow = 576;
 constexpr int kDimV = 128;
 constexpr int kBlockTokens = 64;  // tokens per schedule block = per decode tile
+constexpr int kGroupRows = 128;   // rows per row group (one M=128 tensor-core tile)
 
-// One contiguous run of 64-token blocks of one request, processed by one
-// cluster. Attended positions of the item are [tok_lo, tok_hi).
+// Row groups and rows per group of a request with q_len x heads rows.
+__host__ __device__ inline int row_groups(int q_len, int heads) {
+  return (q_len * heads + kGroupRows - 1) / kGroupRows;
+}
+__host__ __device__ inline int group_rows(int q_len, int heads) {
+  return q_len * heads < kGroupRows ? q_len * heads : kGroupRows;
+}
+
+// Rows of a request: q_len query positions x num_heads heads, row
+// r = i * num_heads + h (q, out and lse are [batch][q_len][heads][...]).
+// Query i attends positions [lo_i, L + i] with L = context_lens[b] and
+// lo_i = 0, or max(0, L + i + 1 - window). A request's rows are cut into
+// groups of at most 128 (one M=128 tile of the tensor core); each (request,
+// row group) is scheduled like a request of its own.
+
+// One contiguous run of 64-token blocks of one (request, row group),
+// processed by one cluster. Attended positions of the item (over all its
+// query positions) are [tok_lo, tok_hi).
 struct WorkItem {
   int b;
   int blk_begin;
@@ -26,14 +43,14 @@ struct WorkItem {
   int tok_lo;
   int tok_hi;
   int cluster;
-  int pad;
+  int row0;      // first row of the row group
 };
 
 struct SplitRequest {
   int b;
   int num_splits;
   int first_partial;
-  int pad;
+  int row0;
 };
 
 struct WsHeader {
@@ -48,7 +65,8 @@ struct WsHeader {
   int num_partials;
   int num_split;
   int planned;        // 1 after a successful plan
-  int pad[5];
+  int q_len;
+  int pad[4];
 };
 
 struct WsLayout {
@@ -57,7 +75,9 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Byte offsets of each region for (batch, heads, clusters).
+// Byte offsets of each region for (scheduled requests, rows per scheduled
+// request, clusters): with q_len > 1, batch x row groups requests of at most
+// 128 rows.
 __host__ __device__ inline WsLayout ws_layout(int batch, int heads, int clusters) {
   WsLayout L;
   size_t off = align_up(sizeof(WsHeader), 256);
@@ -90,6 +110,10 @@ struct DecodeArgs {
   int max_blocks;
   int batch;
   int num_heads;
+  int q_len;         // query positions per request
+  int rows;          // rows per request: q_len * num_heads
+  int group_rows;    // rows per row group: min(rows, 128)
+  int groups;        // row groups per request
   int page_size;
   int window;
   int num_pages;
@@ -145,7 +169,7 @@ cudaError_t launch_kv_write(void* pool, int dtype, int64_t layer_rows, int layer
                             const void* rows, const int64_t* slots, int n, int* status,
                             cudaStream_t stream);
 // plan_merge.cu
-cudaError_t launch_plan(const int32_t* context_lens, int batch, int heads, int page_size,
+cudaError_t launch_plan(const int32_t* context_lens, int batch, int q_len, int heads, int page_size,
                         int window, int clusters, uint8_t* ws, const WsLayout& lay,
                         cudaStream_t stream);
 cudaError_t launch_merge(const DecodeArgs& a, int clusters, cudaStream_t stream);

@@ -1,0 +1,151 @@
+"""Several query positions per request (mla_decode_q): multi-token decode
+(speculative / multi-token-prediction steps, LightLLM PR #1593 "Support dsv4
+model", Summary and Validation) and the absorbed form of chunked prefill
+over the paged latent (vLLM #12639 "[Attention] MLA with chunked prefill",
+Future work), against the oracle.
+
+Request b has L_b cached tokens and q_len new ones at positions L_b ..
+L_b + q_len - 1; query position i attends [start_i, L_b + i]. By that
+definition query i of request b is the single-query decode of a request with
+L_b + i cached tokens over the same page list, which is how the oracle is
+asked (its decode is the pinned plain definition)."""
+import numpy as np
+import pytest
+import torch
+
+import mla_workloads as mw
+import oracle
+from mla_testlib import (TOL_BF16, TOL_FP8, DeviceWorkload, bf16_tensor, check_outputs, f64,
+                         oracle_pool_after_write)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import paged_mla_decode_04_gb300 as m
+    m.load_library()
+    return m
+
+
+def run_q(lib, wl, num_clusters=0, window=None, write=True):
+    """Write the q_len new rows of every request, plan and decode through
+    mla_decode_q; returns (out [B, q_len, H, 512], lse [B, q_len, H])."""
+    window = wl.window if window is None else window
+    dw = DeviceWorkload(wl, lib)
+    if write:
+        lib.kv_write(dw.pool, wl.layer, dw.new_rows, dw.slots, dw.ws)
+    ws = lib.alloc_workspace_q(wl.batch, wl.q_len, wl.num_heads)
+    lib.plan_q(dw.lens, wl.q_len, wl.num_heads, wl.page_size, window, ws, num_clusters)
+    out = torch.full((wl.batch, wl.q_len, wl.num_heads, mw.D_CKV), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")
+    lse = torch.full((wl.batch, wl.q_len, wl.num_heads), float("nan"), dtype=torch.float32, device="cuda")
+    lib.decode_q(dw.pool, wl.layer, dw.q, dw.lens, wl.softmax_scale, ws, out,
+                 block_table=dw.block_table, window=window, lse=lse)
+    torch.cuda.synchronize()
+    assert lib.get_error(ws) == 0
+    assert lib.get_error(dw.ws) == 0
+    return f64(out), lse.cpu().numpy().astype(np.float64)
+
+
+def oracle_q(wl, window=None):
+    """Query i of request b = a single-query request with L_b + i cached
+    tokens and the same pages."""
+    window = wl.window if window is None else window
+    pool = oracle_pool_after_write(wl)
+    B, QL, H = wl.batch, wl.q_len, wl.num_heads
+    q = oracle.bf16_bits_to_f64(wl.q).reshape(B * QL, H, mw.D_ROW)
+    lens = (wl.context_lens.astype(np.int64)[:, None] + np.arange(QL)[None, :]).reshape(-1).astype(np.int32)
+    table = np.repeat(wl.block_table, QL, axis=0)
+    out, lse = oracle.decode(pool, wl.dtype, wl.num_layers, wl.num_pages, wl.page_size, wl.kv_scale,
+                             wl.layer, q, lens, wl.softmax_scale, window, block_table=table)
+    return out.reshape(B, QL, H, mw.D_CKV), lse.reshape(B, QL, H)
+
+
+@pytest.mark.parametrize("heads,q_len", [(16, 2), (16, 4), (32, 3), (64, 2), (16, 8)])
+@pytest.mark.parametrize("clusters", [0, 7])
+def test_multi_token_decode(lib, heads, q_len, clusters):
+    lens = [0, 1, 62, 63, 64, 200, 777, 1500]
+    wl = mw.make("v2lite", num_heads=heads, context_lens=lens, q_len=q_len)
+    out, lse = run_q(lib, wl, num_clusters=clusters)
+    ref_out, ref_lse = oracle_q(wl)
+    check_outputs(out, lse, ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("window", [1, 3, 64, 100])
+def test_multi_token_decode_sliding_window(lib, window):
+    lens = [0, 5, 64, 130, 999]
+    wl = mw.make("v2lite", num_heads=32, context_lens=lens, window=window, q_len=3)
+    out, lse = run_q(lib, wl)
+    ref_out, ref_lse = oracle_q(wl)
+    check_outputs(out, lse, ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("heads,q_len,lens", [
+    (16, 24, [0, 100, 2000]),          # 384 rows: three full row groups
+    (64, 5, [10, 300, 4000]),          # 320 rows: the last group half used
+    (128, 3, [0, 777, 3000]),          # 384 rows at 128 heads
+    (16, 64, [0, 1000]),               # a 64-token chunk, 1024 rows
+])
+@pytest.mark.parametrize("clusters", [0, 3])
+def test_chunked_prefill_absorbed(lib, heads, q_len, lens, clusters):
+    wl = mw.make("v3", num_heads=heads, context_lens=lens, q_len=q_len)
+    out, lse = run_q(lib, wl, num_clusters=clusters)
+    ref_out, ref_lse = oracle_q(wl)
+    check_outputs(out, lse, ref_out, ref_lse)
+
+
+def test_chunked_prefill_fp8_cache(lib):
+    wl = mw.make("fp8", num_heads=32, context_lens=[0, 500, 1300], q_len=6, window=256)
+    out, lse = run_q(lib, wl, num_clusters=5)
+    ref_out, ref_lse = oracle_q(wl)
+    check_outputs(out, lse, ref_out, ref_lse, tol=TOL_FP8)
+
+
+def test_q_len_one_is_mla_decode_bit_for_bit(lib):
+    wl = mw.make("v3", num_heads=128, context_lens=[3000, 17, 900, 2500, 0])
+    dw = DeviceWorkload(wl, lib)
+    ref_out, ref_lse = dw.step()
+    wl1 = mw.make("v3", num_heads=128, context_lens=[3000, 17, 900, 2500, 0])
+    wl1.q = wl1.q.reshape(wl1.batch, 1, wl1.num_heads, mw.D_ROW)
+    out, lse = run_q(lib, wl1, write=True)
+    assert np.array_equal(out[:, 0], ref_out) and np.array_equal(lse[:, 0], ref_lse)
+
+
+def test_causality_with_needles(lib):
+    """Head h of query position i carries a needle dim; the token just after
+    position L + i (which query i + 1 attends) holds the needle. Query i must
+    not pick it up; query i + 1 must return that row exactly."""
+    H, QL = 16, 4
+    lens = [5, 70, 200]
+    wl = mw.make("v2lite", num_heads=H, context_lens=lens, page_size=16, q_len=QL)
+    rng = np.random.default_rng(3)
+    dims = rng.choice(mw.D_ROW, H, replace=False)
+    c = mw.f32_to_bf16_bits(np.float32([2048.0]))[0]
+    one = mw.f32_to_bf16_bits(np.float32([1.0]))[0]
+    wl.q[:] = 0
+    for i in range(QL):
+        wl.q[:, i, np.arange(H), dims] = c
+    wl.pool_bf16[wl.layer][..., dims] = 0
+    wl.new_rows[:, dims] = 0
+    # new token at position L + j (j >= 1) carries the needle of every head
+    for b in range(len(lens)):
+        for j in range(1, QL):
+            wl.new_rows[b * QL + j, dims] = one
+    out, _ = run_q(lib, wl)
+    pool = oracle_pool_after_write(wl)
+    for b, L in enumerate(lens):
+        for i in range(QL):
+            vis = [j for j in range(1, QL) if j <= i]        # needle tokens query i may see
+            row_first = pool[wl.layer, wl.block_table[b, (L + 1) // 16], (L + 1) % 16]
+            if vis:
+                # several needles of equal score: their rows are averaged; with
+                # one (i = 1) the output is that row exactly
+                if len(vis) == 1:
+                    np.testing.assert_array_equal(out[b, i], np.broadcast_to(
+                        oracle.bf16_bits_to_f64(row_first)[:512], out[b, i].shape))
+            else:
+                # query 0 sees no needle: the uniform mean of its L + 1 rows
+                assert not np.array_equal(out[b, 0, 0], oracle.bf16_bits_to_f64(row_first)[:512])
+    ref_out, _ = oracle_q(wl)
+    assert np.abs(out - ref_out).max() <= TOL_BF16 * np.abs(ref_out).max()
