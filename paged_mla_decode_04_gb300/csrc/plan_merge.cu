@@ -25,10 +25,11 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 // A work item costs about this many 64-token blocks beyond its blocks (its
-// epilogue and the pipeline refill when the next item starts): small batches
-// count it in the balance, so clusters that start more requests get fewer
-// blocks.
-constexpr int kItemCostBlocks = 2;
+// epilogue and the pipeline refill when the next item starts; a fit of
+// per-cluster time against blocks and items on the V3-shaped workload gave
+// 3.3): small batches count it in the balance, so clusters that start more
+// requests get fewer blocks.
+constexpr int kItemCostBlocks = 3;
 
 // Block-wide exclusive scan of one int per thread; returns the prefix and
 // writes the block total to *total.

@@ -149,3 +149,48 @@ def test_causality_with_needles(lib):
                 assert not np.array_equal(out[b, 0, 0], oracle.bf16_bits_to_f64(row_first)[:512])
     ref_out, _ = oracle_q(wl)
     assert np.abs(out - ref_out).max() <= TOL_BF16 * np.abs(ref_out).max()
+
+
+def test_rejected_draft_slots_are_rewritten(lib):
+    """A speculative step writes q_len = 4 draft tokens; only 2 are accepted,
+    so the next step starts at L + 2 and writes its 3 new tokens over the
+    rejected slots (L + 2, L + 3) and one more. The pool after both steps is
+    bit-exact against the oracle's two writes in order, and the second
+    step's outputs see the rewritten rows, never the rejected ones."""
+    H = 32
+    lens = [40, 300, 63]
+    wl = mw.make("v2lite", num_heads=H, context_lens=lens, page_size=16, q_len=6)
+    # step 1: 4 draft tokens at L .. L + 3
+    wl1 = mw.make("v2lite", num_heads=H, context_lens=lens, page_size=16, q_len=4)
+    dw = DeviceWorkload(wl, lib)            # the pool with room for L + 5 in every request
+    def slots_of(L_list, q_len):
+        return np.array([int(wl.block_table[b, (L + i) // 16]) * 16 + (L + i) % 16
+                         for b, L in enumerate(L_list) for i in range(q_len)], np.int64)
+    s1 = slots_of(lens, 4)
+    lib.kv_write(dw.pool, wl.layer, bf16_tensor(wl1.new_rows), torch.from_numpy(s1).cuda(), dw.ws)
+    # step 2: 2 accepted, context L + 2, new tokens at L + 2 .. L + 4 (rewrites two rejected slots)
+    lens2 = [L + 2 for L in lens]
+    wl2 = mw.make("v2lite", seed=77, num_heads=H, context_lens=lens2, page_size=16, q_len=3)
+    s2 = slots_of(lens2, 3)
+    lib.kv_write(dw.pool, wl.layer, bf16_tensor(wl2.new_rows), torch.from_numpy(s2).cuda(), dw.ws)
+    ref_pool = wl.pool_bf16.copy()
+    oracle.kv_write(ref_pool, mw.BF16, wl.num_layers, wl.num_pages, 16, 1.0, wl.layer, wl1.new_rows, s1)
+    oracle.kv_write(ref_pool, mw.BF16, wl.num_layers, wl.num_pages, 16, 1.0, wl.layer, wl2.new_rows, s2)
+    got = dw.pool.data.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, ref_pool)
+    # decode step 2 on that pool
+    lens2_t = torch.tensor(lens2, dtype=torch.int32, device="cuda")
+    q2 = bf16_tensor(wl2.q)
+    ws = lib.alloc_workspace_q(len(lens), 3, H)
+    lib.plan_q(lens2_t, 3, H, 16, 0, ws)
+    out = torch.empty(len(lens), 3, H, mw.D_CKV, dtype=torch.bfloat16, device="cuda")
+    lib.decode_q(dw.pool, wl.layer, q2, lens2_t, wl.softmax_scale, ws, out, block_table=dw.block_table)
+    torch.cuda.synchronize()
+    assert lib.get_error(ws) == 0
+    q = oracle.bf16_bits_to_f64(wl2.q).reshape(len(lens) * 3, H, mw.D_ROW)
+    lens_e = np.array([L + i for L in lens2 for i in range(3)], np.int32)
+    table = np.repeat(wl.block_table, 3, axis=0)
+    ref, _ = oracle.decode(ref_pool, mw.BF16, wl.num_layers, wl.num_pages, 16, 1.0, wl.layer, q, lens_e,
+                           wl.softmax_scale, 0, block_table=table)
+    got_out = f64(out).reshape(len(lens) * 3, H, mw.D_CKV)
+    assert np.abs(got_out - ref).max() <= TOL_BF16 * np.abs(ref).max()
