@@ -146,9 +146,9 @@ int mla_decode_plan(const int32_t* context_lens, int batch, int num_heads,
  *        num_heads, page_size and window.
  * num_heads must be 16, 32, 64 or 128 (MLA_ERR_UNSUPPORTED otherwise). The
  * latent width is fixed at 576/512. Arithmetic: fp32 accumulation; the two
- * CTAs that share a work unit exchange their half-dimension partial scores
- * rounded to bf16 (a score's relative error is at most 2^-8 of the larger
- * partial). fp8 pools are dequantised in the kernel, tile by tile: the codes
+ * CTAs that share a work unit exchange their half-dimension partial scores,
+ * scaled to log2 units and rounded to fp16 (relative error at most 2^-11 of
+ * a partial; magnitudes beyond 65504 saturate). fp8 pools are dequantised in the kernel, tile by tile: the codes
  * are exact in f16, q is converted to f16 (exact for |q| in [2^-14, 65504],
  * saturating beyond) and kv_scale multiplies the scores and the output.
  * Launches the split kernel and the merge kernel (which returns at once when

@@ -10,8 +10,8 @@
 // are dense tensor-core contractions.
 //
 // GB300 mapping (measured constraints: a fp32 O for 128 heads x 512 dims
-// fills one SM's tensor memory; a tcgen05.mma costs at least ~55 cycles
-// whatever its shape, so only M=128 instructions pay; SM-to-SM shared memory
+// fills one SM's tensor memory; a tcgen05.mma M=128 K=16 costs ~45 cycles
+// at N=64 and 128 at N=256, so only M=128 instructions pay; SM-to-SM shared memory
 // moves ~13 bytes/cycle, well below an SM's share of HBM). One work unit is a
 // cluster of two CTAs, rank r, that split the latent dimension evenly:
 //   - rank r holds c_kv[256r, 256r+256) and rope[32r, 32r+32) of every row
@@ -20,14 +20,14 @@
 //     of 64-token tiles gathered by TMA (one box per page and chunk), and
 //     the partial S_r = Q_r K_r^T for all heads comes from tcgen05.mma
 //     M=128 x N=64 with A read from TMEM;
-//   - each rank rounds its partial scores to bf16 and sends them to the
-//     peer (st.async, 16 KB per tile), so both ranks form the same sum
-//     bf16(S_0) + bf16(S_1) (fp32 addition commutes) and run the same online
-//     softmax for all heads (base 2, lazy rescale: the reference max moves
-//     only when the running max grows by more than 8, the final 1/l makes
-//     the result exact), each keeping P in its own TMEM. One exchange per
-//     tile and no P traffic. The rounding puts a relative error of at most
-//     2^-8 of the larger half's partial score on each score;
+//   - each rank scales its partial scores to log2 units, rounds them to
+//     fp16 and sends them to the peer (st.async, 16 KB per tile), so both
+//     ranks form the same sum f16(S_0) + f16(S_1) (fp32 addition commutes)
+//     and run the same online softmax for all heads (base 2, lazy rescale:
+//     the reference max moves only when the running max grows by more than
+//     8, the final 1/l makes the result exact), each keeping P in its own
+//     TMEM. One exchange per tile and no P traffic. The rounding puts a
+//     relative error of at most 2^-11 of each partial on each score;
 //   - each rank accumulates O for all heads over its 256 value dims with
 //     tcgen05.mma M=128 x N=256 x K=64, P read from TMEM and V read MN-major
 //     straight from the gathered tile.
@@ -122,7 +122,7 @@ enum Bar {
   kBarDrainPv,
   kNumBars
 };
-static_assert(kNumBars * 8 + 8 <= 1024, "barrier area");
+static_assert(kNumBars * 8 + 8 <= 1024, "barrier area");  // + TMEM address, abort flag
 
 struct Params {
   CUtensorMap kv_wide;    // pool rows [NL*P*ps][576]: bf16 box {64, rows} 128B swizzle; fp8 box {256, rows}
@@ -180,6 +180,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   MLA_TRACER(trc5);  // kernel-level events (thread 0)
   MLA_TRACER(trc);   // this thread's role events
   if (threadIdx.x == 0) MLA_TRACE_EVENT(trc5, 5, kEvKernelStart, 0);
+  if (threadIdx.x == 0) MLA_TRACE_EVENT(trc5, 5, kEvGlobalStart, 0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -227,13 +228,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   // Set-up above overlaps the previous kernel (the plan); from here on the
   // workspace, the pool and q are read.
   pdl_wait();
+  // The cluster's item range is read together with the header (the grid
+  // never has more clusters than the workspace's range table) and used
+  // only if the plan matches.
+  const int cs_lo = cstart[cluster_id], cs_hi = cstart[cluster_id + 1];
   const bool plan_ok = hd->planned == 1 && hd->batch == a.batch && hd->num_heads == a.num_heads &&
                        hd->q_len == a.q_len &&
                        hd->page_size == a.page_size && hd->window == a.window;
   int it_begin = 0, it_end = 0;
   if (plan_ok && cluster_id < hd->num_clusters) {
-    it_begin = cstart[cluster_id];
-    it_end = cstart[cluster_id + 1];
+    it_begin = cs_lo;
+    it_end = cs_hi;
   }
   if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, MLA_STATUS_PLAN_MISMATCH);
   if (threadIdx.x == 0) MLA_TRACE_EVENT(trc5, 5, kEvSetupDone, it_end - it_begin);
@@ -909,9 +914,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) MLA_TRACE_EVENT(trc5, 5, kEvGlobalEnd, 0);
   pdl_launch_dependents();  // the merge may be scheduled as CTAs finish
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   cluster_sync();  // the peer may still address this CTA's shared memory
+  if (threadIdx.x == 0) MLA_TRACE_EVENT(trc5, 5, kEvGlobalExit, 0);
 }
 
 template <bool kFp8>

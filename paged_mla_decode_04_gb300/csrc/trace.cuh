@@ -32,6 +32,9 @@ enum TraceEvent : uint32_t {
   kEvQLoaded,           // QK issuer: q of the item ending before tile g copied to TMEM
   kEvSmXRead,           // softmax: the peer's partials of tile g read and released
   kEvSmPair,            // softmax: the row max of tile g shared with the row's other warp
+  kEvGlobalStart,       // kernel entry, global timer (ns) instead of the SM clock
+  kEvGlobalEnd,         // every role done (before TMEM release), global timer
+  kEvGlobalExit,        // after the final cluster barrier, global timer
 };
 
 constexpr int kTraceRoles = 6;     // producer, QK, PV, softmax (first warp), softmax (last warp), spare
@@ -54,7 +57,10 @@ struct Tracer {
   __device__ __forceinline__ void operator()(int role, uint32_t ev, uint32_t tile) {
     const uint32_t cta = blockIdx.x;
     if (cta >= kTraceCtas || n >= kTraceCap) return;
-    g_trace[cta][role][n] = (clock64() & 0xFFFFFFFFFFull) | (static_cast<uint64_t>(ev & 0xFF) << 40) |
+    uint64_t t;
+    if (ev >= kEvGlobalStart) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    else t = clock64();
+    g_trace[cta][role][n] = (t & 0xFFFFFFFFFFull) | (static_cast<uint64_t>(ev & 0xFF) << 40) |
                             (static_cast<uint64_t>(tile & 0xFFFF) << 48);
     g_trace_n[cta][role] = ++n;
   }
