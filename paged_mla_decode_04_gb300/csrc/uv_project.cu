@@ -4,7 +4,8 @@
 //
 // One CTA per (head, 128 requests): TMA stages 64-wide K chunks of the
 // attention output (K-major A) and of W_UV (N contiguous, MN-major B) in a
-// 4-stage ring; one thread issues tcgen05.mma M=128 N=128 K=16 into a
+// 6-stage ring (the first six W chunks requested before the wait for the
+// previous kernel); one thread issues tcgen05.mma M=128 N=128 K=16 into a
 // 128-column TMEM accumulator; four warps read it back (one TMEM lane per
 // request row) and store bf16.
 #include <cuda_bf16.h>
@@ -16,7 +17,7 @@
 namespace mla {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kKChunks = kDimCkv / 64;        // 8
 constexpr int kABytes = 128 * 128;            // [128 rows][64 k] bf16
 constexpr int kWBytes = 64 * 128;             // [64 k][64 n] bf16
@@ -57,6 +58,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // W_UV does not come from the previous kernel: the first stages' W chunks
+  // are requested before waiting for it, so they stream in while it ends.
+  auto load_w = [&](int kc, int s) {
+    const uint32_t dst = sbase + s * kStageBytes;
+    tma_load_2d(dst + kABytes, &w_map, full(s), 0, h * kDimCkv + kc * 64);
+    tma_load_2d(dst + kABytes + kWBytes, &w_map, full(s), 64, h * kDimCkv + kc * 64);
+  };
+  if (warp == 0 && lane == 0) {
+    for (int kc = 0; kc < kStages; ++kc) {
+      mbar_arrive_expect_tx(full(kc), kStageBytes);
+      load_w(kc, kc);
+    }
+  }
   pdl_wait();  // the attention output is complete
 
   // A wait that runs out in the producer or the issuer stops its loop: the
@@ -65,12 +79,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     for (int kc = 0; kc < kKChunks; ++kc) {
       const int s = kc % kStages, use = kc / kStages;
-      if (!mbar_wait(empty(s), (use & 1) ^ 1, nullptr)) break;
-      mbar_arrive_expect_tx(full(s), kStageBytes);
-      const uint32_t dst = sbase + s * kStageBytes;
-      tma_load_3d(dst, &a_map, full(s), kc * 64, h, b0);
-      tma_load_2d(dst + kABytes, &w_map, full(s), 0, h * kDimCkv + kc * 64);
-      tma_load_2d(dst + kABytes + kWBytes, &w_map, full(s), 64, h * kDimCkv + kc * 64);
+      if (kc >= kStages) {
+        if (!mbar_wait(empty(s), (use & 1) ^ 1, nullptr)) break;
+        mbar_arrive_expect_tx(full(s), kStageBytes);
+        load_w(kc, s);
+      }
+      tma_load_3d(sbase + s * kStageBytes, &a_map, full(s), kc * 64, h, b0);
     }
   } else if (warp == 1 && lane == 0) {
     const uint32_t idesc = idesc_bf16(128, 128, false, true);
