@@ -64,19 +64,18 @@ constexpr int kQNarrowBytes = 128 * 64;             // [128 heads][32 rope dims]
 constexpr int kXBytes = 128 * kTile * 2;            // the peer's partial S of 128 rows, bf16
 constexpr int kF8WideBytes = kTile * 256;           // fp8 tile: [64 tokens][256 c_kv dims], unswizzled
 constexpr int kF8Bytes = kF8WideBytes + kTile * 32;  // + [64 tokens][32 rope dims]
-constexpr int kF8Stages = 2;
+constexpr int kRawOff = kStageBytes - kF8Bytes;      // fp8 pools: the raw tile lands in the slot's back half
 
-// Shared-memory plan of the two variants. bf16 pools: q rope part | 5-stage
-// ring of bf16 tiles | exchange | barriers. fp8 pools: the ring holds the
-// widened f16 tiles (4 stages) and a 2-stage ring of raw fp8 tiles sits
-// beside it.
+// Shared-memory plan of the two variants: q rope part | 5-stage ring of
+// 16-bit tiles | exchange | barriers. fp8 pools: a raw tile (18 KB) lands in
+// the back half of its ring slot and is widened to f16 in place (every code
+// is read into registers before any is overwritten).
 template <bool kFp8>
 struct Cfg {
-  static constexpr int kStages = kFp8 ? 4 : 5;
+  static constexpr int kStages = 5;
   static constexpr int kOffQn = 0;                            // q rope part, staged for TMEM
   static constexpr int kOffKV = kOffQn + kQNarrowBytes;
-  static constexpr int kOffF8 = kOffKV + kStages * kStageBytes;
-  static constexpr int kOffX = kOffF8 + (kFp8 ? kF8Stages * kF8Bytes : 0);  // [2 buffers]
+  static constexpr int kOffX = kOffKV + kStages * kStageBytes;  // [2 buffers]
   static constexpr int kOffBar = kOffX + 2 * kXBytes;
   static constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // barriers + alignment slack
   static constexpr int kThreads = kFp8 ? 512 : 352;
@@ -88,7 +87,7 @@ struct Cfg {
   // 512 threads x 128.
   static constexpr int kRegsIssue = 64, kRegsSoftmax = 176, kRegsCvt = 96;
   static_assert(!kFp8 || kRegsIssue + 2 * kRegsSoftmax + kRegsCvt == 4 * 128, "register split");
-  static_assert(kOffKV % 1024 == 0 && kOffF8 % 1024 == 0 && kOffX % 1024 == 0, "alignment");
+  static_assert(kOffKV % 1024 == 0 && kOffX % 1024 == 0, "alignment");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kStages <= kMaxStages, "barrier arrays");
 };
@@ -99,16 +98,16 @@ constexpr uint32_t kColS = 400;                     // S: [400, 464) fp32
 constexpr uint32_t kColP = 464;                     // P: [464, 496) bf16 pairs
 constexpr float kRescaleThreshold = 8.0f;
 
-static_assert(kStageBytes % 1024 == 0 && kF8Bytes % 1024 == 0, "alignment");
+static_assert(kStageBytes % 1024 == 0 && kF8Bytes % 1024 == 0 && kRawOff % 1024 == 0, "alignment");
 static_assert(2 * kQWideBytes <= kStageBytes, "a ring slot holds two wide q chunks");
 
 enum Bar {
   kBarKvFull = 0,                  // [stages] tile (or q chunks) ready for the tensor core
   kBarKvEmpty = kBarKvFull + kMaxStages,
   kBarRawQ = kBarKvEmpty + kMaxStages,     // [2] fp8 pools: the item's bf16 q chunks landed, not yet f16
-  kBarF8Full = kBarRawQ + 2,               // [kF8Stages] fp8 tile landed
-  kBarF8Empty = kBarF8Full + kF8Stages,    // [kF8Stages] fp8 tile widened
-  kBarQnFull = kBarF8Empty + kF8Stages,    // q rope part ready
+  kBarRawFull = kBarRawQ + 2,              // [stages] fp8 pools: a raw tile landed in the slot
+  kBarCvtRead = kBarRawFull + kMaxStages,  // fp8 pools: every converter holds the raw tile in registers
+  kBarQnFull,                              // q rope part ready
   kBarQnRaw,                       // fp8 pools: q rope part landed, not yet f16
   kBarQnFree,                      // q rope part copied into TMEM
   kBarQDone,                       // every QK of the item complete: TMEM q may be replaced
@@ -149,7 +148,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
   constexpr int kStages = C::kStages;
   constexpr int kOffQn = C::kOffQn;
   constexpr int kOffKV = C::kOffKV;
-  constexpr int kOffF8 = C::kOffF8;
   constexpr int kOffX = C::kOffX;
   constexpr int kOffBar = C::kOffBar;
   // fp8 pools run the tensor core on f16 (q and P converted, codes exact).
@@ -189,10 +187,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     }
     mbar_init(bar(kBarRawQ), 1);
     mbar_init(bar(kBarRawQ + 1), 1);
-    for (int i = 0; i < kF8Stages; ++i) {
-      mbar_init(bar(kBarF8Full + i), 1);
-      mbar_init(bar(kBarF8Empty + i), 128);
-    }
+    for (int i = 0; i < kMaxStages; ++i) mbar_init(bar(kBarRawFull + i), 1);
+    mbar_init(bar(kBarCvtRead), 128);
     mbar_init(bar(kBarQnFull), kFp8 ? 128 : 1);
     mbar_init(bar(kBarQnRaw), 1);
     mbar_init(bar(kBarQnFree), 1);
@@ -253,8 +249,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     // The whole warp walks the tiles; lane 0 issues the copies. Page ids are
     // fetched 32 at a time by the warp (one coalesced load) and handed out
     // by shuffle, so a tile waits on no global load. bf16 pools: tiles go
-    // straight into the ring. fp8 pools: tiles go into the fp8 ring and q
-    // into the ring unconverted; the converter warps finish both.
+    // straight into the ring. fp8 pools: a tile's codes go into the back
+    // half of its ring slot and q into the ring unconverted; the converter
+    // warps finish both.
     const uint64_t kv_policy = l2_policy_evict_first();
     const int64_t layer_row0 = static_cast<int64_t>(a.layer) * a.num_pages * ps;
     const int oob_row = a.num_layers * a.num_pages * ps;  // reads as zeros
@@ -262,7 +259,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     const int boxes = kTile / rows_per_box;
     const uint32_t row_bytes = kFp8 ? 256u + 32u : kWideChunks * 128u + 64u;
     uint32_t sl = 0;     // ring slot
-    uint32_t ft = 0;     // fp8 ring slot
+    uint32_t raw_par = 0;   // fp8 pools: per slot, parity of its next raw-tile phase
+    uint32_t raw_used = 0;  // fp8 pools: slots that have received a raw tile
     int last_qn_item = -1, last_q_item = -1, last_q_chunks = 0;
     uint32_t n_items = 0, gt = 0;
     bool ok = true;
@@ -334,23 +332,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         // Every ring slot is waited for here, in order, for both pool types:
         // a role that skipped slots could run two phases ahead of a slot's
         // barrier, where a parity wait cannot tell the phases apart. For
-        // fp8 pools the converters write the slot after this tile's raw
-        // copy lands, which this wait precedes.
+        // fp8 pools the raw tile lands in the slot's back half and the
+        // converters widen it in place.
         const uint32_t stage = sl % kStages, use = sl / kStages;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarKvEmpty + stage), (use & 1u) ^ 1u, abort_flag));
         uint32_t full_bar, dst0;
         if constexpr (kFp8) {
-          const uint32_t fs = ft % kF8Stages, fu = ft / kF8Stages;
-          ok = ok && __all_sync(0xffffffffu, mbar_wait(bar(kBarF8Empty + fs), (fu & 1u) ^ 1u, abort_flag));
-          full_bar = bar(kBarF8Full + fs);
-          dst0 = sbase + kOffF8 + fs * kF8Bytes;
-          ++ft;
+          full_bar = bar(kBarRawFull + stage);
+          dst0 = sbase + kOffKV + stage * kStageBytes + kRawOff;
         } else {
           full_bar = bar(kBarKvFull + stage);
           dst0 = sbase + kOffKV + stage * kStageBytes;
         }
         ++sl;
         if (!ok) break;
+        if (kFp8) {
+          raw_par ^= 1u << stage;
+          raw_used |= 1u << stage;
+        }
         if (lane == 0) {
           MLA_TRACE_EVENT(trc, 0, kEvSlotAcquired, gt);
           mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(nbox * rows_per_box) * row_bytes);
@@ -386,11 +385,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       }
       if (*abort_flag) {
         // Let every copy already issued land before the CTA can exit (bf16:
-        // ring slots complete KvFull; fp8: tiles complete F8Full and q
-        // chunks RawQ). Each of these waits is itself bounded.
+        // ring slots complete KvFull; fp8: tiles complete RawFull, the last
+        // phase of each slot, and q chunks RawQ). Each of these waits is
+        // itself bounded.
         if (kFp8) {
-          for (uint32_t k = (ft > kF8Stages ? ft - kF8Stages : 0); k < ft; ++k)
-            mbar_wait(bar(kBarF8Full + k % kF8Stages), (k / kF8Stages) & 1u, nullptr);
+          for (int st = 0; st < kStages; ++st)
+            if (raw_used >> st & 1u) mbar_wait(bar(kBarRawFull + st), ((raw_par >> st) & 1u) ^ 1u, nullptr);
           if (last_q_item >= 0)
             for (int h = 0; h < last_q_chunks; ++h) mbar_wait(bar(kBarRawQ + h), last_q_item & 1, nullptr);
         } else {
@@ -522,7 +522,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         st_shared_v4(base + u * 16, x[0], x[1], x[2], x[3]);
       }
     };
-    uint32_t sl = 0, ft = 0, n_items = 0;
+    uint32_t sl = 0, n_items = 0, n_tiles = 0;
+    uint32_t raw_par = 0;  // per slot, parity of its next raw-tile phase
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
       const WorkItem w = items[it];
@@ -538,18 +539,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       q_to_f16(sbase + kOffQn, kQNarrowBytes / 16);
       fence_proxy_async_smem();
       mbar_arrive(bar(kBarQnFull));
-      for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++sl, ++ft) {
+      for (int blk = w.blk_begin; blk < w.blk_end; ++blk, ++sl, ++n_tiles) {
         // The producer waited for this slot's release before the raw copy
-        // that completes F8Full was issued.
+        // that completes RawFull was issued.
         const uint32_t stage = sl % kStages;
-        const uint32_t fs = ft % kF8Stages, fu = ft / kF8Stages;
-        if (!mbar_wait(bar(kBarF8Full + fs), fu & 1u, abort_flag)) { ok = false; break; }
-        const uint32_t src = sbase + kOffF8 + fs * kF8Bytes;
+        if (!mbar_wait(bar(kBarRawFull + stage), (raw_par >> stage) & 1u, abort_flag)) { ok = false; break; }
+        raw_par ^= 1u << stage;
         const uint32_t dst = sbase + kOffKV + stage * kStageBytes;
+        const uint32_t src = dst + kRawOff;
         // 16 codes per unit: 64 rows x 16 units of c_kv, then 64 rows x 2 of
         // rope; 1152 units, nine per thread (units ct + 128 k: eight of
-        // c_kv, one of rope). All nine are loaded first, the raw stage is
-        // released, then widened and stored.
+        // c_kv, one of rope). All nine are loaded first; once every
+        // converter holds its codes the slot is overwritten with the
+        // widened tile.
         static_assert(kTile * 18 == 9 * 128, "nine 16-code units per converter thread");
         uint32_t x[9][4];
 #pragma unroll
@@ -561,11 +563,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           const int r = ct >> 1, c = ct & 1;
           ld_shared_v4(src + kF8WideBytes + r * 32 + c * 16, x[8][0], x[8][1], x[8][2], x[8][3]);
         }
-        // Release the raw slot. The fence orders the generic-proxy reads
-        // above before the slot's next TMA write (async proxy); without it
-        // the copy can land while a read is still in flight.
-        fence_proxy_async_smem();
-        mbar_arrive(bar(kBarF8Empty + fs));
+        mbar_arrive(bar(kBarCvtRead));
+        if (!mbar_wait(bar(kBarCvtRead), n_tiles & 1u, abort_flag)) { ok = false; break; }
 #pragma unroll
         for (int k = 0; k < 9; ++k) {
           uint32_t y[8];
