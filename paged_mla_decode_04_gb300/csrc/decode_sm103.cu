@@ -793,7 +793,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
               uint32_t x[4];
               ld_shared_v4(xq(b) + (j * 32 + lane) * 16, x[0], x[1], x[2], x[3]);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) s2[4 * j + k] = f2_add(f2_from_f16x2(xp[4 * j + k]), f2_from_f16x2(x[k]));
+              for (int k = 0; k < 4; ++k) s2[4 * j + k] = f2_sum_f16x2(xp[4 * j + k], x[k]);
             }
           }
           __syncwarp();

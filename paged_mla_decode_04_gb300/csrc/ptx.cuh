@@ -426,11 +426,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // f16 pair (low half first) to a packed fp32 pair, exactly.
-__device__ __forceinline__ uint64_t f2_from_f16x2(uint32_t v) {
+// f32(a) + f32(b) for each half of two f16 pairs: one conversion and one
+// mixed f16 + f32 addition per half (the same value as converting both and
+// adding: both conversions are exact, the addition rounds once).
+__device__ __forceinline__ uint64_t f2_sum_f16x2(uint32_t a, uint32_t b) {
   float lo, hi;
-  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+  asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t.reg .f32 fl, fh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "cvt.f32.f16 fl, al;\n\tcvt.f32.f16 fh, ah;\n\tadd.rn.f32.f16 %0, bl, fl;\n\tadd.rn.f32.f16 %1, bh, fh;\n\t}"
       : "=f"(lo), "=f"(hi)
-      : "r"(v));
+      : "r"(a), "r"(b));
   return f2_make(lo, hi);
 }
 
