@@ -50,13 +50,6 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar)
                : "memory");
 }
 
-// Arrive on a (possibly remote) cluster barrier, releasing this thread's
-// prior accesses (and those ordered before it, e.g. by __syncwarp) at
-// cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -405,17 +398,6 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
-}
-
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-
-// bf16 pair (low half first) to a packed fp32 pair, exactly.
-__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t v) {
-  return f2_make(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
 // max(a, b, c) in one instruction (three-input max of sm_100 and later).
