@@ -25,6 +25,7 @@ import pytest
 import torch
 
 import mla_workloads as mw
+import oracle
 from mla_testlib import (TOL_BF16, TOL_FP8, DeviceWorkload, check_outputs,
                          oracle_pool_after_write, oracle_step)
 from oracle_fanout import oracle_decode_all
@@ -193,3 +194,38 @@ def test_full_size_every_request(lib, name):
     tol = TOL_FP8 if wl.dtype == mw.FP8_E4M3 else TOL_BF16
     err = check_outputs(out, lse, ref_out, ref_lse, tol)
     print("%s: %d requests, max err %.3e of max|ref|" % (name, wl.batch, err))
+
+
+# ----------------------------------------------------------------- equal scores
+
+@pytest.mark.parametrize("name,window,clusters", [("v3", 0, 0), ("v3", 0, 1), ("v3", 300, 7), ("fp8", 0, 0),
+                                                  ("fp8", 300, 5)])
+def test_equal_scores_give_the_uniform_average(lib, name, window, clusters):
+    """q = 0 makes every score 0: the softmax is uniform, so each head's
+    output is the plain mean of the attended rows' first 512 dims and its
+    lse is ln(n) for n attended positions (the closed form of the
+    definition, MoE-Infinity PR #195 "DeepSeek-V2/V3 paged-attention shim
+    (MLA)", Root causes 4 for the length convention). The mean is taken here
+    directly from the pool, in fp64; the kernel sums n rows with weight 1 in
+    fp32 and rounds the mean to bf16."""
+    lens = [0, 1, 63, 64, 650, 2999]
+    wl = mw.make(name, num_heads=128, context_lens=lens, window=window)
+    wl.q[:] = 0
+    dw = DeviceWorkload(wl, lib)
+    out, lse = dw.step(num_clusters=clusters)
+    assert lib.get_error(dw.ws) == 0
+    pool = oracle_pool_after_write(wl)
+    ps = wl.page_size
+    for b, L in enumerate(lens):
+        lo = max(0, L + 1 - window) if window > 0 else 0
+        pos = np.arange(lo, L + 1)
+        rows = pool[wl.layer, wl.block_table[b, pos // ps], pos % ps][:, :mw.D_CKV]
+        if wl.dtype == mw.BF16:
+            vals = oracle.bf16_bits_to_f64(rows)
+        else:
+            table = np.array([oracle.e4m3_decode(c) for c in range(256)])
+            vals = table[rows] * wl.kv_scale
+        mean = vals.mean(axis=0)
+        err = np.abs(out[b] - mean[None, :])
+        assert np.all(err <= 2.0 ** -8 * np.abs(mean)[None, :] + 1e-6), (b, float(err.max()))
+        np.testing.assert_allclose(lse[b], np.log(len(pos)), rtol=0, atol=2e-6 * max(1.0, np.log(len(pos))))
