@@ -32,7 +32,7 @@
 //     tcgen05.mma M=128 x N=256 x K=64, P read from TMEM and V read MN-major
 //     straight from the gathered tile.
 // TMEM columns: O [0, 256) fp32, q [256, 400), S [400, 464) fp32, P [464,
-// 496) bf16 pairs; S and P are single-buffered (the next QK waits for S to be
+// 496) 16-bit pairs; S and P are single-buffered (the next QK waits for S to be
 // read, the next P for the previous PV).
 // Warp roles per CTA. bf16 pools (352 threads): warp 0 TMA producer, warp 1
 // TMEM owner and QK issuer, warps 2-9 exchange / softmax / correction /
@@ -93,9 +93,9 @@ struct Cfg {
 };
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                       // O: [0, 256) fp32
-constexpr uint32_t kColQ = 256;                     // q: [256, 400) bf16 pairs (wide 128 + rope 16)
+constexpr uint32_t kColQ = 256;                     // q: [256, 400) 16-bit pairs (wide 128 + rope 16)
 constexpr uint32_t kColS = 400;                     // S: [400, 464) fp32
-constexpr uint32_t kColP = 464;                     // P: [464, 496) bf16 pairs
+constexpr uint32_t kColP = 464;                     // P: [464, 496) 16-bit pairs (bf16, f16 for fp8 pools)
 constexpr float kRescaleThreshold = 8.0f;
 
 static_assert(kStageBytes % 1024 == 0 && kF8Bytes % 1024 == 0 && kRawOff % 1024 == 0, "alignment");
@@ -612,10 +612,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     // threads: t and t + 16 hold its tokens [0, 32) and [32, 64) of every
     // tile (and value dims [0, 128) and [128, 256) of this rank's O), so the
     // row max and sum need one shuffle and no other warp. Per tile g: this
-    // rank's partial scores, rounded to bf16, go to the peer (st.async) and
-    // the peer's arrive the same way; both ranks form the same sum
-    // bf16(S_0) + bf16(S_1) (fp32 addition commutes), run the same online
-    // softmax and keep the same P in their own TMEM.
+    // rank's partial scores, scaled to log2 units and rounded to fp16, go to
+    // the peer (st.async) and the peer's arrive the same way; both ranks form
+    // the same sum f16(S_0) + f16(S_1) in fp32 (addition commutes), run the
+    // same online softmax and keep the same P in their own TMEM.
     const int q4 = warp & 3;
     const int half = (warp - C::kSmWarp0) >> 2;     // lane half of the quarter
     const int th = lane >> 4;                       // token half of a tile / value-dim half
@@ -707,9 +707,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     // overlaps the exponentials instead of sitting in this loop.
     int total_tiles = 0;
     for (int it = it_begin; it < it_end; ++it) total_tiles += items[it].blk_end - items[it].blk_begin;
-    // Wait for S(gg), keep this rank's partial (this thread's 32 tokens) as
-    // bf16 pairs in xp, release S, and send the pairs to the peer once it
-    // has read that buffer's previous contents.
+    // Wait for S(gg), keep this rank's partial (this thread's 32 tokens,
+    // log2 units) as fp16 pairs in xp, release S, and send the pairs to the
+    // peer once it has read that buffer's previous contents.
     auto fetch = [&](uint32_t gg, uint32_t* xp) -> bool {
       const uint32_t b = gg & 1u, u = gg >> 1;
       if (!wwait(bar(kBarSFull), gg & 1u)) return false;
@@ -784,7 +784,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
           if (!wwait_cluster(xfull(b), u & 1u)) { ok = false; break; }
           tr(kEvSmXFull, g);
           // Scores as packed fp32 pairs (tokens 2i, 2i+1): both ranks add the
-          // same two bf16 partials.
+          // same two fp16 partials.
           uint64_t s2[kHalf / 2];
           float mxa = -CUDART_INF_F, mxb = -CUDART_INF_F;
           if (valid) {
