@@ -206,6 +206,17 @@ int mla_uv_project(const void* attn_out, const void* w_uv, void* y, int batch,
  * `clear` is nonzero, resets it. Synchronises `stream`: diagnostics only. */
 int mla_get_error(void* workspace, int* code, int clear, void* stream);
 
+/* Self-test of the bounded wait that every kernel of this library uses on
+ * its mbarriers (the published method has no counterpart of this call): one
+ * thread waits for the first phase of a fresh mbarrier, limited to limit_us
+ * microseconds of global time. With arrive == 0 nothing ever completes the
+ * phase, the wait runs out and MLA_STATUS_TIMEOUT is OR-ed into *status (a
+ * device int32); with arrive != 0 the thread arrives first and *status is
+ * left unchanged. Either way the kernel returns and the context stays
+ * usable. Returns MLA_ERR_ARG for a null status or limit_us outside
+ * [1, 1000000]. Asynchronous on `stream`. */
+int mla_selftest_bounded_wait(int arrive, unsigned int limit_us, int32_t* status, void* stream);
+
 /* Allocation-free decode, for callers that cannot allocate device memory at
  * all: code running inside a memory pool or arena that it does not own,
  * plugins whose host forbids cudaMalloc while a graph or a tight memory

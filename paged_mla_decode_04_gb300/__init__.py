@@ -43,7 +43,7 @@ V_HEAD_DIM = 128
 EXPORTED = ["mla_kv_write", "mla_decode_workspace_size", "mla_decode_num_clusters",
             "mla_decode_plan", "mla_decode", "mla_uv_project", "mla_get_error",
             "mla_decode_noalloc", "mla_decode_workspace_size_q", "mla_decode_plan_q",
-            "mla_decode_q"]
+            "mla_decode_q", "mla_selftest_bounded_wait"]
 NOALLOC_SCRATCH_BYTES = 48 << 20
 
 
@@ -84,6 +84,8 @@ def load_library(path: str = LIB_PATH):
     lib.mla_uv_project.restype = I
     lib.mla_get_error.argtypes = [P, ctypes.POINTER(I), I, P]
     lib.mla_get_error.restype = I
+    lib.mla_selftest_bounded_wait.argtypes = [I, ctypes.c_uint, P, P]
+    lib.mla_selftest_bounded_wait.restype = I
     lib.mla_decode_noalloc.argtypes = [ctypes.POINTER(_Pool), I, P, P, P, I, P, I, I, ctypes.c_float,
                                        I, I, P, P, P, P]
     lib.mla_decode_noalloc.restype = I
@@ -260,6 +262,17 @@ def get_error(workspace: torch.Tensor, clear: bool = False, stream=None) -> int:
                                       1 if clear else 0, _stream(stream))
     _check(rc, "mla_get_error")
     return code.value
+
+
+def selftest_bounded_wait(status: torch.Tensor, arrive: bool, limit_us: int, stream=None) -> None:
+    """One thread waits on a fresh mbarrier for at most limit_us; without the
+    arrival the wait runs out and MLA_STATUS_TIMEOUT is OR-ed into status
+    (a device int32 tensor)."""
+    if status.dtype != torch.int32 or status.numel() < 1:
+        raise MlaError("mla_selftest_bounded_wait: status must be a device int32 tensor")
+    rc = load_library().mla_selftest_bounded_wait(1 if arrive else 0, int(limit_us),
+                                                  _dev(status, "status"), _stream(stream))
+    _check(rc, "mla_selftest_bounded_wait")
 
 
 # ----------------------------------------------------------------- several query positions per request

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmla_decode.so")
-SOURCES = ["mla_api.cu", "kv_write.cu", "plan_merge.cu", "decode_sm103.cu", "uv_project.cu"]
+SOURCES = ["mla_api.cu", "kv_write.cu", "plan_merge.cu", "decode_sm103.cu", "uv_project.cu", "selftest.cu"]
 HEADERS = ["ptx.cuh", "mla_internal.h", "trace.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

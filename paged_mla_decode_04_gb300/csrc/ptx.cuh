@@ -98,19 +98,21 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t pa
 }
 
 // Bounded wait for the phase with `parity` to complete. Returns false when
-// the wait ran out or *abort was raised by another role of the CTA. A phase
-// that has already completed is seen by the cheap non-blocking probe
-// (measured: a potentially-blocking try_wait costs ~120 cycles even then);
-// otherwise the thread suspends in try_wait until the phase completes.
+// the wait ran out (after limit_ns of global time) or *abort was raised by
+// another role of the CTA. A phase that has already completed is seen by the
+// cheap non-blocking probe (measured: a potentially-blocking try_wait costs
+// ~120 cycles even then); otherwise the thread suspends in try_wait until the
+// phase completes.
 template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t n = 1;; ++n) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((n & 255u) == 0) {
       if (abort && *abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) return false;
+      if (global_ns() - t0 > limit_ns) return false;
     }
   }
 }

@@ -54,6 +54,12 @@ def test_host_argument_checks_need_no_gpu(lib):
     base = (ctypes.addressof(buf) + 255) // 256 * 256
     assert lib.mla_uv_project(ctypes.c_void_p(base), ctypes.c_void_p(base), ctypes.c_void_p(base), 4, 16,
                               ctypes.c_void_p(base + 8), None) == -3
+    # the bounded-wait self-test refuses a null status word and limits outside [1 us, 1 s]
+    lib.mla_selftest_bounded_wait.restype = ctypes.c_int
+    lib.mla_selftest_bounded_wait.argtypes = [ctypes.c_int, ctypes.c_uint, ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.mla_selftest_bounded_wait(0, 1000, None, None) == -1
+    assert lib.mla_selftest_bounded_wait(0, 0, ctypes.c_void_p(base), None) == -1
+    assert lib.mla_selftest_bounded_wait(0, 1000001, ctypes.c_void_p(base), None) == -1
 
 
 def test_product_package_does_not_touch_the_oracle():
