@@ -194,3 +194,28 @@ def test_rejected_draft_slots_are_rewritten(lib):
                            wl.softmax_scale, 0, block_table=table)
     got_out = f64(out).reshape(len(lens) * 3, H, mw.D_CKV)
     assert np.abs(got_out - ref).max() <= TOL_BF16 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("name,q_len,clusters", [("v3", 2, 0), ("v3", 4, 0), ("fp8", 2, 0), ("v2lite", 4, 0)])
+def test_full_size_multi_token_decode_sampled(lib, name, q_len, clusters):
+    """Multi-token decode at the full-size workloads' shapes (V3: 128 heads,
+    so q_len x 128 rows run as q_len row groups, each split across clusters;
+    fp8; V2-Lite: 16 heads, one row group), in the launch configuration of
+    the bench (all clusters). Every query position of sampled requests
+    against the oracle."""
+    wl = mw.make(name, q_len=q_len)
+    out, lse = run_q(lib, wl, num_clusters=clusters)
+    B, QL, H = wl.batch, wl.q_len, wl.num_heads
+    sample = sorted(set([0, B // 3, B // 2, B - 1]))
+    # fp8: the oracle quantises only the sampled requests' pages
+    pages = None if wl.dtype == mw.BF16 else np.concatenate(
+        [wl.block_table[b][wl.block_table[b] >= 0] for b in sample])
+    pool = oracle_pool_after_write(wl, pages=pages)
+    q = oracle.bf16_bits_to_f64(wl.q)[sample].reshape(len(sample) * QL, H, mw.D_ROW)
+    lens = (wl.context_lens.astype(np.int64)[sample][:, None] + np.arange(QL)[None, :]).reshape(-1).astype(np.int32)
+    table = np.repeat(wl.block_table[sample], QL, axis=0)
+    ref_out, ref_lse = oracle.decode(pool, wl.dtype, wl.num_layers, wl.num_pages, wl.page_size, wl.kv_scale,
+                                     wl.layer, q, lens, wl.softmax_scale, wl.window, block_table=table)
+    tol = TOL_FP8 if wl.dtype != mw.BF16 else TOL_BF16
+    check_outputs(out[sample].reshape(-1, H, mw.D_CKV), lse[sample].reshape(-1, H),
+                  ref_out, ref_lse, tol=tol)
