@@ -219,3 +219,15 @@ def test_full_size_multi_token_decode_sampled(lib, name, q_len, clusters):
     tol = TOL_FP8 if wl.dtype != mw.BF16 else TOL_BF16
     check_outputs(out[sample].reshape(-1, H, mw.D_CKV), lse[sample].reshape(-1, H),
                   ref_out, ref_lse, tol=tol)
+
+
+@pytest.mark.parametrize("ps,window,clusters", [(16, 100, 7), (32, 0, 3), (128, 40, 0)])
+def test_fp8_pages_windows_and_splits_with_several_positions(lib, ps, window, clusters):
+    """fp8 pools at page sizes below and above the 64-token tile (several raw
+    copies per ring slot, widened in place), with a window and split items,
+    for three query positions per request."""
+    wl = mw.make("fp8", num_heads=32, context_lens=[0, 15, 64, 333, 1500], page_size=ps, window=window,
+                 q_len=3)
+    out, lse = run_q(lib, wl, num_clusters=clusters)
+    ref_out, ref_lse = oracle_q(wl)
+    check_outputs(out, lse, ref_out, ref_lse, tol=TOL_FP8)
