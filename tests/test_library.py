@@ -69,3 +69,17 @@ def test_product_package_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in src.lower(), f
+
+
+def test_tracing_tool_reads_the_event_enum():
+    """The trace tool's event ids come from the kernel's header (a rename or
+    a new event there cannot leave the tool reading the wrong records)."""
+    from paged_mla_decode_04_gb300 import tracing
+    ids = tracing.event_ids()
+    assert ids["KernelStart"] == 1 and ids["SetupDone"] == 2
+    assert sorted(ids.values()) == list(range(1, len(ids) + 1))
+    for name in ["SlotAcquired", "TileIssued", "QkTileReady", "QkSFree", "QkIssued", "SmSFull", "SmSent",
+                 "SmXFull", "SmComputed", "SmPvDone", "SmOFixed", "PvOFixed", "PvIssued", "GlobalStart",
+                 "GlobalEnd"]:
+        assert name in ids
+    assert tracing.summarize({}, ids) == ""
