@@ -231,3 +231,22 @@ def test_fp8_pages_windows_and_splits_with_several_positions(lib, ps, window, cl
     out, lse = run_q(lib, wl, num_clusters=clusters)
     ref_out, ref_lse = oracle_q(wl)
     check_outputs(out, lse, ref_out, ref_lse, tol=TOL_FP8)
+
+
+@pytest.mark.parametrize("name", ["v2lite", "fp8"])
+def test_csr_page_lists_equal_block_tables_for_several_positions(lib, name):
+    """The CSR page lists (kv_indptr / kv_indices) give the same bits as the
+    block table for several query positions per request."""
+    wl = mw.make(name, num_heads=32, context_lens=[0, 63, 64, 700, 2100], q_len=3)
+    out_t, lse_t = run_q(lib, wl, num_clusters=5)
+    dw = DeviceWorkload(wl, lib)
+    lib.kv_write(dw.pool, wl.layer, dw.new_rows, dw.slots, dw.ws)
+    ws = lib.alloc_workspace_q(wl.batch, wl.q_len, wl.num_heads)
+    lib.plan_q(dw.lens, wl.q_len, wl.num_heads, wl.page_size, wl.window, ws, 5)
+    out = torch.empty(wl.batch, wl.q_len, wl.num_heads, mw.D_CKV, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(wl.batch, wl.q_len, wl.num_heads, dtype=torch.float32, device="cuda")
+    lib.decode_q(dw.pool, wl.layer, dw.q, dw.lens, wl.softmax_scale, ws, out, page_indptr=dw.indptr,
+                 page_ids=dw.ids, window=wl.window, lse=lse)
+    torch.cuda.synchronize()
+    assert lib.get_error(ws) == 0
+    assert np.array_equal(f64(out), out_t) and np.array_equal(lse.cpu().numpy().astype(np.float64), lse_t)
