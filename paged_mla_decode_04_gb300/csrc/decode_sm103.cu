@@ -17,7 +17,9 @@
 //   - rank r holds c_kv[256r, 256r+256) and rope[32r, 32r+32) of every row
 //     (288 dims) and of q. Per item its q slice goes to TMEM (tcgen05.cp,
 //     staged through two ring slots), so shared memory holds a 5-stage ring
-//     of 64-token tiles gathered by TMA (one box per page and chunk), and
+//     of 64-token tiles gathered by TMA (for pages of 64 tokens or more one
+//     3-D box covers the rank's four c_kv chunks, else one box per page and
+//     chunk; the rope part is one more box), and
 //     the partial S_r = Q_r K_r^T for all heads comes from tcgen05.mma
 //     M=128 x N=64 with A read from TMEM;
 //   - each rank scales its partial scores to log2 units, rounds them to
@@ -39,9 +41,9 @@
 // epilogue, warp 10 PV issuer. fp8 pools (512 threads, one role group per
 // warpgroup so that setmaxnreg can move registers to the softmax warps):
 // warps 0, 1, 2 producer, QK issuer, PV issuer (warp 3 idle), warps 4-11
-// softmax, warps 12-15 widen fp8 tiles to f16. A softmax warp w works on 16
-// lanes of TMEM lane quarter w & 3; a head's row belongs to two threads,
-// tokens [0, 32) and [32, 64) of each tile.
+// softmax, warps 12-15 widen fp8 tiles to f16 in place in their ring slot.
+// A softmax warp w works on 16 lanes of TMEM lane quarter w & 3; a head's row
+// belongs to two threads, tokens [0, 32) and [32, 64) of each tile.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
