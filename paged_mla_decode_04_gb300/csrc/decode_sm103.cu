@@ -610,14 +610,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     // ------------------------------------------------------------ exchange, softmax, correction, epilogue
     if constexpr (kFp8) setmaxnreg_inc<C::kRegsSoftmax>();
     // Warp w works on 16 rows (heads) of TMEM lane quarter q4 = w & 3: the
-    // first four softmax warps on its lanes 0-15, the next four on 16-31. A row belongs to two
-    // threads: t and t + 16 hold its tokens [0, 32) and [32, 64) of every
-    // tile (and value dims [0, 128) and [128, 256) of this rank's O), so the
-    // row max and sum need one shuffle and no other warp. Per tile g: this
-    // rank's partial scores, scaled to log2 units and rounded to fp16, go to
-    // the peer (st.async) and the peer's arrive the same way; both ranks form
-    // the same sum f16(S_0) + f16(S_1) in fp32 (addition commutes), run the
-    // same online softmax and keep the same P in their own TMEM.
+    // first four softmax warps on its lanes 0-15, the next four on 16-31. A
+    // row belongs to two threads: t and t + 16 hold its tokens [0, 32) and
+    // [32, 64) of every tile (and value dims [0, 128) and [128, 256) of this
+    // rank's O), so the row max and sum need one shuffle and no other warp.
+    // Per tile g: this rank's partial scores, scaled to log2 units and
+    // rounded to fp16, go to the peer (st.async) and the peer's arrive the
+    // same way; both ranks form the same sum f16(S_0) + f16(S_1) in fp32
+    // (addition commutes), run the same online softmax and keep the same P
+    // in their own TMEM.
     const int q4 = warp & 3;
     const int half = (warp - C::kSmWarp0) >> 2;     // lane half of the quarter
     const int th = lane >> 4;                       // token half of a tile / value-dim half
