@@ -53,6 +53,10 @@ struct SplitRequest {
   int row0;
 };
 
+// How the plan cut the work (WsHeader::schedule).
+constexpr int kScheduleCut = 0;     // blocks of all requests concatenated, cut into equal ranges
+constexpr int kSchedulePacked = 1;  // long requests split, pieces paired largest with smallest
+
 struct WsHeader {
   int status;  // sticky MLA_STATUS_* bits
   int batch;
@@ -66,7 +70,8 @@ struct WsHeader {
   int num_split;
   int planned;        // 1 after a successful plan
   int q_len;
-  int pad[4];
+  int schedule;       // kScheduleCut or kSchedulePacked
+  int pad[3];
 };
 
 struct WsLayout {

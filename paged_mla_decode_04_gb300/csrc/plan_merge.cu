@@ -9,7 +9,10 @@
 // functionality"), i.e. 64-token blocks s_b/64 .. L_b/64. The blocks of all
 // requests, concatenated in request order, are cut into C equal contiguous
 // ranges, one per cluster; a request crossing a range boundary becomes
-// several items whose partial (O, lse) are merged afterwards. With several
+// several items whose partial (O, lse) are merged afterwards. Batches of up
+// to 1024 requests also get a packed schedule (only requests heavier than a
+// cluster's share are split; pieces dealt largest-first) and keep whichever
+// has the lower estimated cost. With several
 // query positions per request (q_len > 1) request b attends [s_b, L_b +
 // q_len - 1] over all its queries, and each of its row groups is scheduled
 // like a request of its own (virtual request v = b * groups + group).
@@ -25,15 +28,19 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 // A work item costs about this many 64-token blocks beyond its blocks (its
-// epilogue and the pipeline refill when the next item starts; a fit of
-// per-cluster time against blocks and items on the V3-shaped workload gave
-// 3.3): small batches count it in the balance, so clusters that start more
-// requests get fewer blocks.
-constexpr int kItemCostBlocks = 3;
+// epilogue and the pipeline refill when the next item starts: in an event
+// trace of the V3-shaped workload, clusters with one more item ended 4-5
+// blocks' time later): small batches count it in the balance, so clusters
+// that start more requests get fewer blocks.
+constexpr int kItemCostBlocks = 4;
+// Pieces (and clusters) the packed schedule handles in shared memory.
+constexpr int kPackMax = 256;
 
 // Block-wide exclusive scan of one int per thread; returns the prefix and
-// writes the block total to *total.
-__device__ int block_excl_scan(int v, int* total, int* smem32) {
+// writes the block total to *total. The plan runs once per step on one CTA
+// whose time goes mostly to latency, so its helpers are called, not inlined:
+// one copy of their code serves every call.
+__device__ __noinline__ int block_excl_scan(int v, int* total, int* smem32) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = static_cast<int>(blockDim.x >> 5);
   int x = v;
@@ -58,6 +65,42 @@ __device__ int block_excl_scan(int v, int* total, int* smem32) {
   *total = smem32[31];
   __syncthreads();
   return warp_prefix + x - v;
+}
+
+// The same for three counts at once, 21 bits each (every count and every sum
+// stays below 2^21): one pass of 64-bit shuffles instead of three passes.
+__device__ __noinline__ unsigned long long block_excl_scan3(unsigned long long v, unsigned long long* total,
+                                               unsigned long long* smem64) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) smem64[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = lane < nwarps ? smem64[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    smem64[lane] = w;
+  }
+  __syncthreads();
+  const unsigned long long warp_prefix = warp ? smem64[warp - 1] : 0;
+  *total = smem64[31];
+  __syncthreads();
+  return warp_prefix + x - v;
+}
+constexpr unsigned long long kField = (1ull << 21) - 1;
+// items, partial slots (items of a split request) and split requests
+__device__ __forceinline__ unsigned long long counts3(int items) {
+  const unsigned long long k = static_cast<unsigned>(items);
+  return items > 1 ? k | (k << 21) | (1ull << 42) : k;
 }
 
 // The products below stay under 2^32 whenever T * C does (T blocks, C <= 1024
@@ -104,11 +147,29 @@ __global__ void __launch_bounds__(kPlanThreads)
   };
 
   if (V <= static_cast<int>(blockDim.x)) {
-    // One request per thread, everything in registers: no pass through
-    // global memory between the scans. Request b weighs its n_b blocks plus
-    // kItemCostBlocks; the weights are concatenated in request order and cut
-    // into C equal ranges; a request's blocks sit after its extra weight.
+    // One request per thread, everything in registers or shared memory: no
+    // pass through global memory between the scans. Two schedules are
+    // formed and the cheaper one is written:
+    //  - cut: request b weighs its n_b blocks plus kItemCostBlocks; the
+    //    weights are concatenated in request order and cut into C equal
+    //    ranges (a request's blocks sit after its extra weight), so nearly
+    //    every range boundary splits a request;
+    //  - packed: a request heavier than a cluster's share of the weight is
+    //    split into that many near-equal pieces, the pieces are ranked by
+    //    size (largest first) and dealt in two rounds: rank r < C to
+    //    cluster r, rank C + j to cluster C - 1 - j, the least loaded after
+    //    the first round. Only the split requests leave partials.
+    // Cost of a schedule, in sixteenths of a block: 16 x its largest cluster
+    // load (blocks plus kItemCostBlocks per item) plus, per partial, its
+    // rows / 128: writing a 128-row fp32 partial and reading it back in the
+    // merge takes about a sixteenth of a block's time over the whole GPU.
     __shared__ int last_cluster[kPlanThreads];
+    __shared__ unsigned long long smem64[32];
+    __shared__ __align__(16) int piece_size[kPackMax + 4];
+    __shared__ int piece_rank[kPackMax];
+    __shared__ int by_rank[kPackMax];
+    __shared__ int max_load_packed;
+    if (tid == 0) max_load_packed = 0;  // published by the scans' barriers
     int L = 0, s = 0, first = 0, n = 0;
     const int vb = tid / G, vg = tid - (tid / G) * G;  // request and row group of this thread
     if (tid < V) range_of(vb, L, s, first, n);
@@ -116,6 +177,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     const int off = block_excl_scan(tid < V ? n + kItemCostBlocks : 0, &T32, smem32) + kItemCostBlocks;
     const long long T = T32;
     const long long C = T > 0 ? (T < C_req ? T : C_req) : 1;
+    const int Ci = static_cast<int>(C);
     int cf = 0, cl = -1, ns = 0;
     if (tid < V) {
       cf = cluster_of(off, T, C);
@@ -123,42 +185,149 @@ __global__ void __launch_bounds__(kPlanThreads)
       ns = cl - cf + 1;
     }
     last_cluster[tid] = cl;
-    int t_items, t_part, t_split;
-    const int item0 = block_excl_scan(ns, &t_items, smem32);
-    const int part0 = block_excl_scan(ns > 1 ? ns : 0, &t_part, smem32);
-    const int split0 = block_excl_scan(ns > 1 ? 1 : 0, &t_split, smem32);
+    auto cut_range = [&](int k, long long& lo, long long& hi) {
+      const int c = cf + k;
+      lo = max(static_cast<long long>(off), range_lo(c, T, C));
+      hi = min(static_cast<long long>(off) + n, range_lo(c + 1, T, C));
+    };
+    // Pieces of this request in the packed schedule: its weight over a
+    // cluster's share, rounded up (at most one per block).
+    int kv = 0;
     if (tid < V) {
-      for (int k = 0; k < ns; ++k) {
-        const int c = cf + k;
-        const long long lo = max(static_cast<long long>(off), range_lo(c, T, C));
-        const long long hi = min(static_cast<long long>(off) + n, range_lo(c + 1, T, C));
-        WorkItem w;
-        w.b = vb;
-        w.blk_begin = first + static_cast<int>(lo - off);
-        w.blk_end = first + static_cast<int>(hi - off);
-        w.slot = ns > 1 ? part0 + k : -1;
-        w.tok_lo = s;
-        w.tok_hi = L + q_len;
-        w.cluster = c;
-        w.row0 = vg * kGroupRows;
-        items[item0 + k] = w;
-      }
-      if (ns > 1) {
-        SplitRequest r;
-        r.b = vb;
-        r.num_splits = ns;
-        r.first_partial = part0;
-        r.row0 = vg * kGroupRows;
-        split[split0] = r;
-      }
-      // First item of each cluster after the previous request's last one
-      // (clusters whose range holds no block of any request get an empty
-      // range at this request's first item).
-      const int prev = tid > 0 ? last_cluster[tid - 1] : -1;
-      for (int c = prev + 1; c <= cl; ++c) cstart[c] = item0 + (c > cf ? c - cf : 0);
+      const long long num = static_cast<long long>(n + kItemCostBlocks) * C + T - 1;
+      kv = num < (1ll << 32) ? static_cast<int>(static_cast<unsigned>(num) / static_cast<unsigned>(T))
+                             : static_cast<int>(num / T);
+      kv = min(max(kv, 1), n);
     }
-    const int cl_last = V > 0 ? last_cluster[V - 1] : -1;
-    for (int c = cl_last + 1 + tid; c <= C_req; c += blockDim.x) cstart[c] = t_items;
+    // Items, partial slots and split requests of both schedules: prefixes
+    // (this request's first of each) and totals.
+    unsigned long long tot_cut, tot_pk;
+    const unsigned long long ex_cut = block_excl_scan3(counts3(ns), &tot_cut, smem64);
+    const unsigned long long ex_pk = block_excl_scan3(counts3(kv), &tot_pk, smem64);
+    const int item0 = static_cast<int>(ex_cut & kField), part0 = static_cast<int>((ex_cut >> 21) & kField),
+              split0 = static_cast<int>(ex_cut >> 42);
+    const int t_items = static_cast<int>(tot_cut & kField), t_part = static_cast<int>((tot_cut >> 21) & kField),
+              t_split = static_cast<int>(tot_cut >> 42);
+    const int pitem0 = static_cast<int>(ex_pk & kField), ppart0 = static_cast<int>((ex_pk >> 21) & kField),
+              psplit0 = static_cast<int>(ex_pk >> 42);
+    const int p_items = static_cast<int>(tot_pk & kField), p_part = static_cast<int>((tot_pk >> 21) & kField),
+              p_split = static_cast<int>(tot_pk >> 42);
+    // The packed schedule is formed only where it can pay: it fits (at most
+    // two pieces per cluster) and the partials it saves are worth at least
+    // half a block. The cut's largest load is its share rounded up plus one
+    // item cost (a cluster starts inside one request).
+    const long long rows = min(q_len * H, kGroupRows);
+    bool packed = false;
+    if (V > 0 && Ci <= kPackMax && p_items <= 2 * Ci && p_items <= kPackMax &&
+        ((t_part - p_part) * rows >> 7) >= 8) {  // the same for every thread
+      if (tid < V) {
+        const int base = n / kv, rem = n - base * kv;
+        for (int i = 0; i < kv; ++i) piece_size[pitem0 + i] = base + (i < rem ? 1 : 0);
+      }
+      if (tid < 3) piece_size[p_items + tid] = -1;  // pad to whole int4 (sizes are >= 1)
+      __syncthreads();
+      // Rank of each piece (larger first, then by index); sizes by rank.
+      // Sizes are read four at a time and counted in two chains.
+      for (int p = tid; p < p_items; p += blockDim.x) {
+        const int sz = piece_size[p];
+        int ra = 0, rb = 0;
+        const int4* ps4 = reinterpret_cast<const int4*>(piece_size);
+#pragma unroll 1
+        for (int q4 = 0; q4 < (p_items + 3) >> 2; ++q4) {
+          const int4 v = ps4[q4];
+          const int q = 4 * q4;
+          ra += (v.x > sz || (v.x == sz && q < p)) ? 1 : 0;
+          rb += (v.y > sz || (v.y == sz && q + 1 < p)) ? 1 : 0;
+          ra += (v.z > sz || (v.z == sz && q + 2 < p)) ? 1 : 0;
+          rb += (v.w > sz || (v.w == sz && q + 3 < p)) ? 1 : 0;
+        }
+        const int rank = ra + rb;
+        piece_rank[p] = rank;
+        by_rank[rank] = sz;
+      }
+      __syncthreads();
+      // Cluster c holds rank c and, for the last p_items - C clusters, rank
+      // 2C - 1 - c.
+      int mx = 0;
+      for (int c = tid; c < min(p_items, Ci); c += blockDim.x) {
+        const int r2 = 2 * Ci - 1 - c;
+        mx = max(mx, by_rank[c] + kItemCostBlocks + (r2 < p_items ? by_rank[r2] + kItemCostBlocks : 0));
+      }
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if ((tid & 31) == 0) atomicMax(&max_load_packed, mx);
+      __syncthreads();
+      const long long share = (T + C - 1) / C;
+      const long long cost_cut = 16ll * (share + kItemCostBlocks) + ((t_part * rows) >> 7);
+      const long long cost_packed = 16ll * max_load_packed + ((p_part * rows) >> 7);
+      packed = cost_packed < cost_cut;
+      if (packed) {
+        // Cluster c holds its first-round piece, then its second-round one
+        // (the last n2 clusters have one).
+        const int n1 = min(p_items, Ci), n2 = p_items - n1;
+        auto first_item = [&](int cc) { return min(cc, n1) + max(0, cc - (Ci - n2)); };
+        if (tid < V) {
+          const int base = n / kv, rem = n - base * kv;
+          int b0 = first;
+          for (int i = 0; i < kv; ++i) {
+            const int size = base + (i < rem ? 1 : 0);
+            const int rank = piece_rank[pitem0 + i];
+            WorkItem w;
+            w.b = vb;
+            w.blk_begin = b0;
+            w.blk_end = b0 + size;
+            w.slot = kv > 1 ? ppart0 + i : -1;
+            w.tok_lo = s;
+            w.tok_hi = L + q_len;
+            w.cluster = rank < Ci ? rank : 2 * Ci - 1 - rank;
+            w.row0 = vg * kGroupRows;
+            items[first_item(w.cluster) + (rank < Ci ? 0 : 1)] = w;
+            b0 += size;
+          }
+          if (kv > 1) {
+            SplitRequest r;
+            r.b = vb;
+            r.num_splits = kv;
+            r.first_partial = ppart0;
+            r.row0 = vg * kGroupRows;
+            split[psplit0] = r;
+          }
+        }
+        for (int cc = tid; cc <= C_req; cc += blockDim.x) cstart[cc] = cc <= Ci ? first_item(cc) : p_items;
+      }
+    }
+    if (!packed) {
+      if (tid < V) {
+        for (int k = 0; k < ns; ++k) {
+          long long lo, hi;
+          cut_range(k, lo, hi);
+          WorkItem w;
+          w.b = vb;
+          w.blk_begin = first + static_cast<int>(lo - off);
+          w.blk_end = first + static_cast<int>(hi - off);
+          w.slot = ns > 1 ? part0 + k : -1;
+          w.tok_lo = s;
+          w.tok_hi = L + q_len;
+          w.cluster = cf + k;
+          w.row0 = vg * kGroupRows;
+          items[item0 + k] = w;
+        }
+        if (ns > 1) {
+          SplitRequest r;
+          r.b = vb;
+          r.num_splits = ns;
+          r.first_partial = part0;
+          r.row0 = vg * kGroupRows;
+          split[split0] = r;
+        }
+        // First item of each cluster after the previous request's last one
+        // (clusters whose range holds no block of any request get an empty
+        // range at this request's first item).
+        const int prev = tid > 0 ? last_cluster[tid - 1] : -1;
+        for (int c = prev + 1; c <= cl; ++c) cstart[c] = item0 + (c > cf ? c - cf : 0);
+      }
+      const int cl_last = V > 0 ? last_cluster[V - 1] : -1;
+      for (int c = cl_last + 1 + tid; c <= C_req; c += blockDim.x) cstart[c] = t_items;
+    }
     __syncthreads();
     if (tid == 0) {
       if (bad_len) atomicOr(&hd->status, MLA_STATUS_BAD_LENGTH);
@@ -167,11 +336,12 @@ __global__ void __launch_bounds__(kPlanThreads)
       hd->q_len = q_len;
       hd->page_size = ps;
       hd->window = window;
-      hd->num_clusters = static_cast<int>(C);
+      hd->num_clusters = Ci;
       hd->total_blocks = static_cast<int>(T);
-      hd->num_items = t_items;
-      hd->num_partials = t_part;
-      hd->num_split = t_split;
+      hd->num_items = packed ? p_items : t_items;
+      hd->num_partials = packed ? p_part : t_part;
+      hd->num_split = packed ? p_split : t_split;
+      hd->schedule = packed ? kSchedulePacked : kScheduleCut;
       hd->planned = 1;
     }
     return;
@@ -275,6 +445,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     hd->num_items = n_items;
     hd->num_partials = n_part;
     hd->num_split = n_split;
+    hd->schedule = kScheduleCut;
     hd->planned = 1;
   }
 }
@@ -371,11 +542,16 @@ __global__ void __launch_bounds__(32 * kMergeHeadsPerBlock)
 cudaError_t launch_plan(const int32_t* context_lens, int batch, int q_len, int heads, int page_size,
                         int window, int clusters, uint8_t* ws, const WsLayout& lay,
                         cudaStream_t stream) {
-  // Small batches: one thread per scheduled (request, row group), whole
-  // warps, every step in registers; larger ones: 1024 threads looping.
+  // Small batches: one thread per scheduled (request, row group) and at
+  // least one per piece of the packed schedule (at most two per cluster),
+  // whole warps; larger ones: 1024 threads looping.
   const int G = row_groups(q_len, heads);
   const int V = batch * G;
-  const int threads = V <= kPlanThreads ? ((V + 31) / 32 * 32 > 32 ? (V + 31) / 32 * 32 : 32) : kPlanThreads;
+  int threads = kPlanThreads;
+  if (V <= kPlanThreads) {
+    const int pieces = 2 * clusters < kPackMax ? 2 * clusters : kPackMax;
+    threads = (max(max(V, pieces), 1) + 31) / 32 * 32;
+  }
   return launch_pdl(plan_kernel, dim3(1), dim3(threads), 0, stream, context_lens, batch, q_len, G, heads, page_size,
                     window, clusters, ws, lay);
 }
