@@ -112,11 +112,15 @@ int mla_decode_num_clusters(void);
  * SGLang PR #32972, Correction: the plan writes into a buffer the caller
  * keeps, so a captured decode reads what the last plan wrote).
  * Reads context_lens (device, [batch] int32, tokens cached before this step),
- * splits the attended tokens of all requests into 64-token blocks, and cuts
- * the concatenated block sequence into `num_clusters` equal contiguous
- * ranges, one per cluster; a request whose blocks span several ranges is
- * split and its partial results are merged by mla_decode. The schedule
- * depends only on the lengths. Must be re-run whenever context_lens,
+ * splits the attended tokens of all requests into 64-token blocks, and
+ * deals the blocks to `num_clusters` clusters. Either the concatenated block
+ * sequence is cut into equal contiguous ranges, one per cluster, or (batches
+ * of up to 1024 requests, when it is estimated cheaper) only requests
+ * heavier than a cluster's share are split into near-equal pieces and the
+ * pieces are dealt largest first, at most two per cluster. A request split
+ * over several clusters has its partial results merged by mla_decode. The
+ * schedule depends only on the lengths and is the same on every call with
+ * the same arguments. Must be re-run whenever context_lens,
  * batch, num_heads, page_size or window change, before mla_decode.
  *   num_clusters: 0 = mla_decode_num_clusters(); 1 = no split at all;
  *                 values above mla_decode_num_clusters() are clamped to it.
