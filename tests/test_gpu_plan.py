@@ -24,8 +24,17 @@ import pytest
 import torch
 
 import mla_workloads as mw
+from mla_testlib import DeviceWorkload, check_outputs, oracle_step
+from test_gpu_multi_query import oracle_q, run_q
 
 pytestmark = pytest.mark.gpu
+
+# 24 requests of 319-3195 tokens (a lognormal-like mix): at 16 clusters the
+# equal cut would leave 22 fp32 partials, the packed schedule 8, with the
+# same largest cluster load; the plan picks the packed one, single- and
+# two-position alike (128 rows per request either way).
+MIXED_LENS = [1849, 2840, 2008, 455, 339, 943, 1644, 1285, 3195, 1522, 1408, 539, 414, 2543, 931, 1588,
+              343, 663, 364, 522, 1693, 319, 619, 1009]
 
 HEADER = ["status", "batch", "num_heads", "page_size", "window", "num_clusters", "total_blocks",
           "num_items", "num_partials", "num_split", "planned", "q_len", "schedule"]
@@ -144,3 +153,27 @@ def test_equal_lengths_keep_the_cut(lib):
     so the cut (every cluster the same share) is kept."""
     head = plan_and_check(lib, mw.make("fp8").context_lens, 128)
     assert head["schedule"] == CUT
+
+
+def test_packed_schedule_decode_matches_the_oracle(lib):
+    """Decode under the packed schedule (whole requests written directly,
+    the heavy ones split and merged): every request against the oracle."""
+    wl = mw.make("v3", context_lens=MIXED_LENS)
+    dw = DeviceWorkload(wl, lib)
+    out, lse = dw.step(num_clusters=16)
+    head = read_schedule(lib, dw.ws, wl.batch)[0]
+    assert head["schedule"] == PACKED and 0 < head["num_partials"] < 22
+    ref_out, ref_lse = oracle_step(wl)
+    check_outputs(out, lse, ref_out, ref_lse)
+    assert lib.get_error(dw.ws) == 0
+
+
+def test_packed_schedule_with_two_positions_matches_the_oracle(lib):
+    """The same mix with two query positions per request at 64 heads (one
+    128-row group per request), through mla_decode_q."""
+    wl = mw.make("v3", num_heads=64, context_lens=MIXED_LENS, q_len=2)
+    head = plan_and_check(lib, MIXED_LENS, 64, q_len=2, clusters=16)
+    assert head["schedule"] == PACKED
+    out, lse = run_q(lib, wl, num_clusters=16)
+    ref_out, ref_lse = oracle_q(wl)
+    check_outputs(out, lse, ref_out, ref_lse)
