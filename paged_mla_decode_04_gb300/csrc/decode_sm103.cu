@@ -106,8 +106,12 @@ static_assert(2 * kQWideBytes <= kStageBytes, "a ring slot holds two wide q chun
 enum Bar {
   kBarKvFull = 0,                  // [stages] tile (or q chunks) ready for the tensor core
   kBarKvEmpty = kBarKvFull + kMaxStages,
-  kBarRawQ = kBarKvEmpty + kMaxStages,     // [2] fp8 pools: the item's bf16 q chunks landed, not yet f16
-  kBarRawFull = kBarRawQ + 2,              // [stages] fp8 pools: a raw tile landed in the slot
+  // [stages] fp8 pools: the slot's raw contents landed (a tile's codes, or
+  // two bf16 q chunks), not yet f16. One barrier per slot: its phases follow
+  // the slot's uses, which the slot's release keeps in order. (A barrier
+  // shared by all items' q chunks could complete twice before the widening
+  // warps wait on it when an item has a single tile.)
+  kBarRawFull = kBarKvEmpty + kMaxStages,
   kBarCvtRead = kBarRawFull + kMaxStages,  // fp8 pools: every converter holds the raw tile in registers
   kBarQnFull,                              // q rope part ready
   kBarQnRaw,                       // fp8 pools: q rope part landed, not yet f16
@@ -187,8 +191,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       mbar_init(bar(kBarKvFull + i), kFp8 ? 128 : 1);  // fp8: every converter thread arrives
       mbar_init(bar(kBarKvEmpty + i), 1);
     }
-    mbar_init(bar(kBarRawQ), 1);
-    mbar_init(bar(kBarRawQ + 1), 1);
     for (int i = 0; i < kMaxStages; ++i) mbar_init(bar(kBarRawFull + i), 1);
     mbar_init(bar(kBarCvtRead), 128);
     mbar_init(bar(kBarQnFull), kFp8 ? 128 : 1);
@@ -261,9 +263,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
     const int boxes = kTile / rows_per_box;
     const uint32_t row_bytes = kFp8 ? 256u + 32u : kWideChunks * 128u + 64u;
     uint32_t sl = 0;     // ring slot
-    uint32_t raw_par = 0;   // fp8 pools: per slot, parity of its next raw-tile phase
-    uint32_t raw_used = 0;  // fp8 pools: slots that have received a raw tile
-    int last_qn_item = -1, last_q_item = -1, last_q_chunks = 0;
+    uint32_t raw_par = 0;   // fp8 pools: per slot, parity of its next raw phase (tile or q chunks)
+    uint32_t raw_used = 0;  // fp8 pools: slots that have received a raw copy
+    int last_qn_item = -1;
     uint32_t n_items = 0, gt = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
@@ -280,15 +282,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
         const uint32_t stage = sl % kStages, use = sl / kStages;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarKvEmpty + stage), (use & 1u) ^ 1u, abort_flag));
         if (ok && lane == 0) {
-          const uint32_t fb = kFp8 ? bar(kBarRawQ + h) : bar(kBarKvFull + stage);
+          const uint32_t fb = kFp8 ? bar(kBarRawFull + stage) : bar(kBarKvFull + stage);
           mbar_arrive_expect_tx(fb, 2 * kQWideBytes);
           for (int c = 0; c < 2; ++c)
             tma_load_2d(sbase + kOffKV + stage * kStageBytes + c * kQWideBytes, &p.q_wide, fb,
                         wide_x + 64 * (2 * h + c), w.b * a.rows + w.row0);
         }
-        if (ok) {
-          last_q_item = static_cast<int>(n_items);
-          last_q_chunks = h + 1;
+        if (ok && kFp8) {
+          raw_par ^= 1u << stage;
+          raw_used |= 1u << stage;
         }
       }
       if (!ok) break;
@@ -387,14 +389,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       }
       if (*abort_flag) {
         // Let every copy already issued land before the CTA can exit (bf16:
-        // ring slots complete KvFull; fp8: tiles complete RawFull, the last
-        // phase of each slot, and q chunks RawQ). Each of these waits is
-        // itself bounded.
+        // ring slots complete KvFull; fp8: tiles and q chunks complete
+        // RawFull, the last phase of each slot). Each of these waits is itself
+        // bounded.
         if (kFp8) {
           for (int st = 0; st < kStages; ++st)
             if (raw_used >> st & 1u) mbar_wait(bar(kBarRawFull + st), ((raw_par >> st) & 1u) ^ 1u, nullptr);
-          if (last_q_item >= 0)
-            for (int h = 0; h < last_q_chunks; ++h) mbar_wait(bar(kBarRawQ + h), last_q_item & 1, nullptr);
         } else {
           for (uint32_t k = (sl > kStages ? sl - kStages : 0); k < sl; ++k)
             mbar_wait(bar(kBarKvFull + k % kStages), (k / kStages) & 1u, nullptr);
@@ -525,13 +525,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads,
       }
     };
     uint32_t sl = 0, n_items = 0, n_tiles = 0;
-    uint32_t raw_par = 0;  // per slot, parity of its next raw-tile phase
+    uint32_t raw_par = 0;  // per slot, parity of its next raw phase (tile or q chunks)
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_items) {
       const WorkItem w = items[it];
       for (int h = 0; h < 2; ++h, ++sl) {
         const uint32_t stage = sl % kStages;
-        if (!mbar_wait(bar(kBarRawQ + h), n_items & 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(bar(kBarRawFull + stage), (raw_par >> stage) & 1u, abort_flag)) { ok = false; break; }
+        raw_par ^= 1u << stage;
         q_to_f16(sbase + kOffKV + stage * kStageBytes, 2 * kQWideBytes / 16);
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarKvFull + stage));
