@@ -34,7 +34,7 @@ import mla_workloads as mw  # noqa: E402
 # from an ncu capture, keyed by workload and by the digest of the decode
 # kernel's sources at capture time (decode_source_digest): the figure is
 # printed only for the kernel it was measured on, null for any other.
-MEASURED_TRAFFIC = {("v3", "7807bdfde0b765f2"): 365.87e6, ("fp8", "7807bdfde0b765f2"): 667.75e6}
+MEASURED_TRAFFIC = {("v3", "1b30d15897f2214c"): 365.50e6, ("fp8", "1b30d15897f2214c"): 666.80e6}
 DECODE_SOURCES = ["decode_sm103.cu", "ptx.cuh", "mla_internal.h", "trace.cuh"]
 METRIC = "paged MLA decode µs/step, KV GB/s & TFLOP/s as % of GB300 roofline"
 UNIT = "us/step"
