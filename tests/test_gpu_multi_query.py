@@ -196,13 +196,20 @@ def test_rejected_draft_slots_are_rewritten(lib):
     assert np.abs(got_out - ref).max() <= TOL_BF16 * np.abs(ref).max()
 
 
-@pytest.mark.parametrize("name,q_len,clusters", [("v3", 2, 0), ("v3", 4, 0), ("fp8", 2, 0), ("v2lite", 4, 0)])
+@pytest.mark.parametrize("name,q_len,clusters", [("v3", 2, 0), ("v3", 4, 0), ("fp8", 2, 0), ("fp8", 2, 75),
+                                                 ("v2lite", 4, 0)])
 def test_full_size_multi_token_decode_sampled(lib, name, q_len, clusters):
     """Multi-token decode at the full-size workloads' shapes (V3: 128 heads,
     so q_len x 128 rows run as q_len row groups, each split across clusters;
     fp8; V2-Lite: 16 heads, one row group), in the launch configuration of
     the bench (all clusters). Every query position of sampled requests
-    against the oracle."""
+    against the oracle.
+
+    fp8 over 75 clusters: the schedule then starts a cluster with a
+    single-block split piece followed by more items, under full load, the
+    case in which a barrier shared by all items' q chunks could complete two
+    phases before the widening warps waited on it (now one barrier per ring
+    slot); run_q also requires a clean status word (no timed-out wait)."""
     wl = mw.make(name, q_len=q_len)
     out, lse = run_q(lib, wl, num_clusters=clusters)
     B, QL, H = wl.batch, wl.q_len, wl.num_heads
